@@ -1,0 +1,107 @@
+"""Number formats used by the oracle: BF16 and FP8 E4M3 ("e4m3fn"), written from their
+format definitions.  Test infrastructure only (see the package docstring).
+
+BF16: 1 sign bit, 8 exponent bits (bias 127), 7 stored mantissa bits -- the top half
+of an IEEE float32.  Conversion from float32 rounds to nearest, ties to even.
+
+E4M3 (the "fn" variant used by the FP8 dispatch of the DeepEP page and by the combine
+fake-quant of the Mega-MoE page): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
+no infinities.  Exponent field 0 holds subnormals m * 2^-9; exponent field 15 with
+mantissa 7 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.  Encoding rounds
+to nearest, ties to even, and saturates finite values beyond 448 to +-448 ("satfinite").
+
+Pinned in tests/test_oracle_formats.py against torch's CPU casts (library routines) on
+exhaustive or large seeded sets, and against the definition's special cases.
+"""
+import numpy as np
+
+E4M3_MAX = 448.0
+E4M3_MIN_NORMAL = 2.0 ** -6
+E4M3_SUBNORMAL_STEP = 2.0 ** -9
+
+
+def f32_to_bf16_bits(x):
+    """float32 array -> uint16 BF16 bit patterns, round to nearest even.
+
+    The 16 discarded low bits are compared with the halfway point 0x8000; above it, or
+    at it with an odd kept part, the kept part is incremented (a carry into the
+    exponent is the correct result, including overflow to infinity).  NaN stays NaN.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    kept = u >> 16
+    low = u & 0xFFFF
+    up = (low > 0x8000) | ((low == 0x8000) & ((kept & 1) == 1))
+    out = (kept + up.astype(np.uint64)).astype(np.uint32)
+    nan = np.isnan(x)
+    out = np.where(nan, (kept & 0x8000) | 0x7FC0, out)
+    return out.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b):
+    """uint16 BF16 bit patterns -> float32 (exact)."""
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_round(x):
+    """float32 -> nearest-even BF16 value, returned as float32."""
+    return bf16_bits_to_f32(f32_to_bf16_bits(x))
+
+
+def e4m3_decode(codes):
+    """uint8 E4M3 codes -> float32 values (exact); codes 0x7F / 0xFF decode to NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    ex = (c >> 3) & 0xF
+    man = c & 0x7
+    sub = man * E4M3_SUBNORMAL_STEP
+    norm = (1.0 + man / 8.0) * np.exp2(ex - 7.0)
+    mag = np.where(ex == 0, sub, norm)
+    mag = np.where((ex == 15) & (man == 7), np.nan, mag)
+    return (sign * mag).astype(np.float32)
+
+
+def e4m3_encode(x):
+    """float32 array -> uint8 E4M3 codes: round to nearest even, saturate to +-448.
+
+    Works in float64, where every float32 input and every scaling by a power of two is
+    exact.  The spacing of E4M3 values around |x| is 2^-9 below the smallest normal
+    2^-6, else 2^(e-3) for 2^e <= |x| < 2^(e+1); |x| / spacing is rounded half to even
+    (np.rint) and scaled back.  A value that rounds past 448 is clamped to 448.  The
+    code is then read off the rounded value, so a rounding carry into the next binade
+    is handled by construction.
+    """
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, a)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
+    e = ex.astype(np.int64) - 1               # a in [2^e, 2^(e+1))
+    step = np.where(a < E4M3_MIN_NORMAL, E4M3_SUBNORMAL_STEP,
+                    np.exp2(np.maximum(e, -6) - 3.0))
+    v = np.rint(a / step) * step
+    v = np.minimum(v, E4M3_MAX)
+    # code from the (exactly representable) rounded magnitude v
+    _, vex = np.frexp(v)
+    ve = vex.astype(np.int64) - 1
+    is_sub = v < E4M3_MIN_NORMAL
+    sub_code = np.rint(v / E4M3_SUBNORMAL_STEP).astype(np.int64)
+    safe_e = np.where(is_sub, 0, ve)
+    man = np.rint((v / np.exp2(safe_e) - 1.0) * 8.0).astype(np.int64)
+    norm_code = ((safe_e + 7) << 3) | man
+    code = np.where(is_sub, sub_code, norm_code)
+    code = np.where(nan, 0x7F, code)
+    code = code | np.where(neg, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def e4m3_round(x):
+    """float32 -> nearest-even, saturated E4M3 value, returned as float32."""
+    return e4m3_decode(e4m3_encode(x))
+
+
+def round_up(x, y):
+    """Smallest multiple of y that is >= x (the tile-count helper of the DeepEP page)."""
+    return ((x + y - 1) // y) * y

@@ -1,0 +1,111 @@
+"""Pins for the oracle's SwiGLU experts and the dense per-token layer reference:
+brute-force scalar loops on tiny inputs, the silu odd-part identity (catches a sign
+error or swapped gate/up halves), and the FP8 reference against the BF16 one."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle.formats import bf16_bits_to_f32, f32_to_bf16_bits
+from oracle.moe_ref import layer_reference, max_rel_err, route_topk, swiglu_expert
+
+
+def brute_expert(x, w13, w2):
+    """Scalar loops: y_j = sum_i W2[j, i] * silu(sum_h Wg[i, h] x_h) * (sum_h Wu[i, h] x_h)."""
+    I = len(w13) // 2
+    H = len(x)
+    h = []
+    for i in range(I):
+        g = sum(float(w13[i][c]) * float(x[c]) for c in range(H))
+        u = sum(float(w13[I + i][c]) * float(x[c]) for c in range(H))
+        h.append(g / (1.0 + math.exp(-g)) * u)
+    return [sum(float(w2[j][i]) * h[i] for i in range(I)) for j in range(len(w2))]
+
+
+def test_expert_matches_scalar_loops():
+    rng = np.random.default_rng(1)
+    H, I = 7, 5
+    x = rng.standard_normal((3, H))
+    w13 = rng.standard_normal((2 * I, H))
+    w2 = rng.standard_normal((H, I))
+    y = swiglu_expert(x, w13, w2)
+    for m in range(3):
+        assert np.allclose(y[m], brute_expert(x[m], w13, w2), rtol=1e-12, atol=1e-12)
+
+
+def test_silu_odd_part_identity():
+    """silu(g) - silu(-g) = g, so negating the gate rows changes the output by
+    W_down (g * u): a bilinear form with no silu in it."""
+    rng = np.random.default_rng(2)
+    H, I = 32, 24
+    x = rng.standard_normal((10, H))
+    w13 = rng.standard_normal((2 * I, H))
+    w2 = rng.standard_normal((H, I))
+    neg = w13.copy()
+    neg[:I] *= -1
+    g = x @ w13[:I].T
+    u = x @ w13[I:].T
+    diff = swiglu_expert(x, w13, w2) - swiglu_expert(x, neg, w2)
+    assert np.allclose(diff, (g * u) @ w2.T, rtol=1e-10, atol=1e-10)
+
+
+def brute_layer(x, idx, w, w13, w2, shared):
+    T, K = idx.shape
+    out = np.zeros((T, x.shape[1]))
+    for t in range(T):
+        acc = [0.0] * x.shape[1]
+        any_valid = False
+        for k in range(K):
+            e = idx[t, k]
+            if e < 0:
+                continue
+            any_valid = True
+            y = brute_expert(x[t], w13[e], w2[e])
+            acc = [a + float(w[t, k]) * b for a, b in zip(acc, y)]
+        if any_valid and shared is not None:
+            y = brute_expert(x[t], shared[0], shared[1])
+            acc = [a + b for a, b in zip(acc, y)]
+        out[t] = acc
+    return out
+
+
+@pytest.mark.parametrize("with_shared", [False, True])
+def test_layer_reference_matches_brute_force(with_shared):
+    rng = np.random.default_rng(3)
+    T, H, I, E, K = 9, 6, 4, 5, 2
+    xb = f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    idx, w = route_topk(rng.standard_normal((T, E)).astype(np.float32), K)
+    idx[4, 1] = -1
+    idx[6, :] = -1
+    w13 = f32_to_bf16_bits(rng.standard_normal((E, 2 * I, H)).astype(np.float32))
+    w2 = f32_to_bf16_bits(rng.standard_normal((E, H, I)).astype(np.float32))
+    shared = None
+    if with_shared:
+        shared = (f32_to_bf16_bits(rng.standard_normal((2 * I, H)).astype(np.float32)),
+                  f32_to_bf16_bits(rng.standard_normal((H, I)).astype(np.float32)))
+    ref = layer_reference(xb, idx, w, w13, w2, shared=shared)
+    f = lambda a: bf16_bits_to_f32(a).astype(np.float64)
+    brute = brute_layer(f(xb), idx, w, f(w13), f(w2),
+                        None if shared is None else (f(shared[0]), f(shared[1])))
+    assert np.allclose(ref, brute, rtol=1e-12, atol=1e-12)
+    assert np.all(ref[6] == 0)
+    # a token subset gives the same rows
+    sub = layer_reference(xb, idx, w, w13, w2, shared=shared, tokens=[8, 2, 4])
+    assert np.allclose(sub, ref[[8, 2, 4]], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_reference_error_is_the_fp8_rounding_error():
+    """The FP8 reference differs from the BF16 one by E4M3's own rounding error: four
+    quantised operands (x, W13, h, W2), each with a uniform relative rounding error of
+    rms 2^-4/sqrt(3) = 3.6%, give about sqrt(4) * 3.6% = 7% rms on the output."""
+    rng = np.random.default_rng(4)
+    T, H, I, E, K = 16, 256, 256, 4, 2
+    xb = f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    idx, w = route_topk(rng.random((T, E)).astype(np.float32), K)
+    w13 = f32_to_bf16_bits((rng.standard_normal((E, 2 * I, H)) / math.sqrt(H)).astype(np.float32))
+    w2 = f32_to_bf16_bits((rng.standard_normal((E, H, I)) / math.sqrt(I)).astype(np.float32))
+    ref = layer_reference(xb, idx, w, w13, w2)
+    ref8 = layer_reference(xb, idx, w, w13, w2, fp8=True)
+    rms = np.sqrt(((ref8 - ref) ** 2).mean() / (ref ** 2).mean())
+    assert 0.03 < rms < 0.10
+    assert max_rel_err(ref8, ref) < 0.15

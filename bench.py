@@ -1,0 +1,450 @@
+"""Benchmark of the MoE layer hot path on GB300: one step = one pass of the whole layer
+(route -> permute -> grouped GEMM gate/up + SwiGLU -> grouped GEMM down -> combine)
+over one batch of the prefill workload (T = 8192 tokens in a 16384-row bucket,
+H = 7168, I = 2048, E = 256, top-8, one shared expert, BF16, Zipf(1.1) router skew).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  `value` is layer tokens/s with inputs resident in HBM;
+`e2e` is the same metric through moe_layer_forward with the step's inputs copied from
+pinned host memory and its output copied back inside the timed region.  The per-kernel
+breakdown (and the roofline of the dominant kernel) comes from a second timed pass that
+issues the same steps through the per-step C calls with CUDA events between them.
+Inputs are synthetic (seeded); the weights (22.6 GB) are far larger than L2, so every
+step streams them from HBM without an explicit flush.
+
+`--impl reference` times the CPU oracle (plain numpy, as it stands) on a bounded sample
+of the same workload on the host cores.  Under torchrun (N > 1) each rank runs an
+independent batch on its own GPU (token-sharded replicas, no collective in the data
+path); timing is the max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from combine_moe_route_softmax_gb300 import synth  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ distributed glue
+def dist_env():
+    """(rank, world, local_rank) from torchrun's environment (1-process defaults)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed, rank):
+    """Each rank draws its own batch (weak scaling); the weights are shared (same seed)."""
+    return seed + 1000 * rank
+
+
+# ---------------------------------------------------------------------- peaks/clocks
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax = float(p[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------- our arm
+def workload_state(w, seed, device):
+    import combine_moe_route_softmax_gb300 as moe
+    logits = synth.router_logits(w, seed, device=device)
+    x = synth.hidden(w, seed, device=device)
+    w13, w2, s13, s2 = synth.expert_weights(w, 0, device=device)   # weights shared by all ranks
+    kw = dict(w13=w13, w2=w2, shared_w13=s13, shared_w2=s2)
+    dtype = moe.MOE_BF16
+    if w.dtype == "e4m3":
+        q13, c13 = moe.moe_quantize_weight_fp8(w13)
+        q2, c2 = moe.moe_quantize_weight_fp8(w2)
+        kw = dict(w13=q13, w2=q2, w13_scales=c13, w2_scales=c2)
+        if w.shared:
+            qs13, cs13 = moe.moe_quantize_weight_fp8(s13)
+            qs2, cs2 = moe.moe_quantize_weight_fp8(s2)
+            kw.update(shared_w13=qs13, shared_w2=qs2, shared_w13_scales=cs13, shared_w2_scales=cs2)
+        del w13, w2, s13, s2
+        dtype = moe.MOE_E4M3
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, **kw)
+    st = dict(layer=layer, logits=logits, x=x,
+              idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
+              wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
+              out=torch.empty(w.T, w.H, dtype=torch.bfloat16, device=device),
+              n=torch.tensor([w.T_valid], dtype=torch.int32, device=device),
+              status=torch.zeros(1, dtype=torch.int32, device=device))
+    return st
+
+
+def layer_step(st, x=None, logits=None, out=None):
+    st["layer"].forward(st["x"] if x is None else x, st["out"] if out is None else out, st["idx"], st["wt"],
+                        logits=st["logits"] if logits is None else logits, num_tokens=st["n"],
+                        dev_status=st["status"])
+
+
+STAGES = ("route", "permute", "gemm_gate_up", "gemm_down", "combine")
+
+
+def staged_step(st, w, events):
+    """The same step as moe_layer_forward, issued call by call with an event after each."""
+    import combine_moe_route_softmax_gb300 as moe
+    L = moe.lib()
+    lay = st["layer"]
+    v, d = lay.views, lay.desc
+    s = torch.cuda.current_stream().cuda_stream
+    nseg = d.E + d.has_shared
+    tw = lay.tensors
+    p = lambda t: None if t is None else t.data_ptr()
+    events[0].record()
+    assert L.moe_route_topk(p(st["logits"]), d.T, d.E, d.K, p(st["n"]), p(st["idx"]), p(st["wt"]), s) == 0
+    events[1].record()
+    scratch_bytes = L.moe_permute_workspace_bytes(d.T, d.K, d.E, d.has_shared)
+    scratch = st.setdefault("scratch", torch.empty(scratch_bytes, dtype=torch.uint8, device=st["x"].device))
+    assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp, v.xp_scales,
+                         v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch), scratch_bytes,
+                         p(st["status"]), s) == 0
+    events[2].record()
+    assert L.moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), p(tw[4]), d.E,
+                              p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales, p(st["status"]),
+                              s) == 0
+    events[3].record()
+    assert L.moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]), d.E,
+                              p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]), s) == 0
+    events[4].record()
+    assert L.moe_combine(v.y, v.inv_map, p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None, v.shared_map,
+                         None, p(st["out"]), s) == 0
+    events[5].record()
+
+
+KERNELS_PER_STEP = {"route": 1, "permute": 4, "gemm_gate_up": 1, "gemm_down": 1, "combine": 1}
+
+
+def algorithmic_work(w, st):
+    """Bytes / FLOPs each stage must move or compute for this batch (read once after
+    warm-up, outside the timed regions)."""
+    lay = st["layer"]
+    d = lay.desc
+    cu = lay.view("cu_seqlens", (d.E + d.has_shared + 1,), torch.int32).cpu().numpy()
+    counts = np.diff(cu)
+    n_routed = int(cu[d.E])
+    n_total = int(cu[-1])
+    n_tok = int(counts[d.E]) if d.has_shared else int((st["idx"] >= 0).any(dim=1).sum().item())
+    T, K, H, I, E = d.T, d.K, d.H, d.I, d.E
+    esz = 1 if w.dtype == "e4m3" else 2
+    act = H * (1 + 4 / 128) if esz == 1 else H * 2
+    experts_touched = int((counts[:E] > 0).sum()) + (1 if d.has_shared else 0)
+    return {
+        "route": {"bytes": T * E * 4 + T * K * 8},
+        "permute": {"bytes": n_tok * H * 2 + n_total * act + T * K * 4 * 2 + v_cap(d) * 4 + T * 4},
+        "gemm_gate_up": {"flops": 2.0 * n_total * H * 2 * I, "bytes": experts_touched * 2 * I * H * esz},
+        "gemm_down": {"flops": 2.0 * n_total * I * H, "bytes": experts_touched * H * I * esz},
+        "combine": {"bytes": (n_routed + (n_total - n_routed)) * H * 2 + T * K * 8 + T * H * 2},
+        "_rows": {"n_routed": n_routed, "n_total": n_total, "tokens": n_tok, "experts_touched": experts_touched},
+    }
+
+
+def v_cap(d):
+    return d.T * d.K + (d.T if d.has_shared else 0)
+
+
+def run_ours(args, rank, world, local_rank):
+    import combine_moe_route_softmax_gb300 as moe
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    st = workload_state(w, rank_seed(0, rank), device)
+    for _ in range(args.warmup):
+        layer_step(st)
+    torch.cuda.synchronize()
+    assert st["status"].item() == 0, f"device status {st['status'].item()}"
+    work = algorithmic_work(w, st)
+
+    # --- timed region 1: the layer with inputs resident in HBM
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            layer_step(st)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    clocks = clk.summary()
+
+    # --- timed region 2: per-kernel breakdown (same kernels, events between the calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        staged_step(st, w, ev[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    stage_ms = {}
+    for j, name in enumerate(STAGES):
+        t = statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+        stage_ms[name] = max_over_ranks(t, world, device)
+
+    # --- timed region 3: end to end through moe_layer_forward with host buffers
+    h_logits = st["logits"].cpu().pin_memory()
+    h_x = st["x"].cpu().pin_memory()
+    h_out = torch.empty(st["out"].shape, dtype=torch.bfloat16).pin_memory()
+    d_logits, d_x = torch.empty_like(st["logits"]), torch.empty_like(st["x"])
+    for _ in range(2):
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        layer_step(st, x=d_x, logits=d_logits)
+        h_out.copy_(st["out"], non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        layer_step(st, x=d_x, logits=d_logits)
+        h_out.copy_(st["out"], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    assert st["status"].item() == 0
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    tok = w.T_valid * world
+    kernels = {}
+    for name in STAGES:
+        k = {"ms": round(stage_ms[name], 4)}
+        wk = work[name]
+        if "flops" in wk:
+            k["tflops"] = round(wk["flops"] / (stage_ms[name] * 1e-3) / 1e12, 1)
+            k["frac_tc"] = round(k["tflops"] / peaks["bf16_tflops_sustained"], 3)
+        gbs = wk["bytes"] / (stage_ms[name] * 1e-3) / 1e9
+        k["gbs"] = round(gbs, 1)
+        k["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
+        kernels[name] = k
+    dom = max(("gemm_gate_up", "gemm_down"), key=lambda n: stage_ms[n])
+    bound = "tensor" if w.dtype == "bf16" else "hbm"
+    if bound == "tensor":
+        achieved = work[dom]["flops"] / (stage_ms[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work[dom]["bytes"] / (stage_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get(f"{args.workload}:{dom}")
+    cpu = cpu_baseline(w, tokens=args.cpu_tokens) if world == 1 and not args.no_cpu_baseline else None
+    line = {
+        "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
+        "value": round(tok / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "e4m3",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) random-init weights, Zipf(1.1) router bias)",
+        "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
+                               f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
+                   "tokens_per_step": w.T_valid, "parallelism": f"token-sharded replicas x{world}",
+                   "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
+        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "kernels": kernels,
+        "rows": work["_rows"],
+        "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+        "e2e": {"value": round(tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
+                "d2h_bytes_per_step": h_out.numel() * 2},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(w, tokens, seed=0):
+    """Inputs for the oracle on a sample of the workload's tokens (host, untimed): the
+    sample's logits and activations and the BF16 weights of every expert it routes to."""
+    from oracle import moe_ref as ref
+    logits = synth.router_logits(w, seed).numpy()
+    x = synth.hidden(w, seed)
+    toks = np.arange(tokens)
+    idx, _ = ref.route_topk(logits[toks], w.K)
+    experts = sorted(set(idx.reshape(-1).tolist()))
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    w13 = {e: bits(synth.expert_w13(w, 0, e)) for e in experts}
+    w2 = {e: bits(synth.expert_w2(w, 0, e)) for e in experts}
+    shared = (bits(synth.expert_w13(w, 0, w.E)), bits(synth.expert_w2(w, 0, w.E))) if w.shared else None
+    return logits[toks], bits(x[:tokens]), w13, w2, shared
+
+
+def oracle_step(w, sample):
+    """The oracle's layer on the sample: route, permute, fp64 experts and the sum."""
+    from oracle import moe_ref as ref
+    logits, xb, w13, w2, shared = sample
+    idx, wt = ref.route_topk(logits, w.K)
+    ref.permute(idx, w.E, with_shared=w.shared)
+    return ref.layer_reference(xb, idx, wt, w13, w2, shared=shared)
+
+
+def cpu_baseline(w, tokens=8, reps=1):
+    sample = oracle_sample(w, tokens)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(w, sample)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{tokens} tokens of the {w.name} workload through the numpy oracle (route, permute, fp64 "
+                      f"experts, fixed-order sum); {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    sample = oracle_sample(w, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_step(w, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, sample)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = round(args.ref_tokens / dt, 3)
+    line = {
+        "impl": "reference",
+        "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
+        "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
+                               f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
+                   "tokens_per_step": args.ref_tokens},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "kind": "oracle", "cores": os.cpu_count(),
+                         "sample": f"{args.ref_tokens} tokens per step through the numpy oracle"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

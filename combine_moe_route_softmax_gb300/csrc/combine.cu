@@ -1,0 +1,190 @@
+// Combine: gather each token's K expert rows through the inverse map, router-weight
+// them, optionally fake-quantise each weighted row to E4M3 with a constant scale, sum in
+// float32 in ascending slot order starting from +0, add the shared expert's row last and
+// unquantised, round once to BF16.
+//
+// Mega-MoE page: combine_quantizer "fake-quantizes the router-weighted per-(token, top-k
+// slot) rows ..., then sums them again in the kernel's order (ascending slot, FP32 from
+// zero, one BF16 rounding; a fused shared expert's slot last and unquantized)".  The same
+// page's layout self-check compares a re-sum with the kernel output bit for bit; inside a
+// captured graph the check runs on the device (moe_combine_verify, which reports through
+// a status word instead of asserting).
+//
+// Every float op is an explicit round-to-nearest intrinsic (__fmul_rn / __fadd_rn /
+// __fdiv_rn) so the compiler cannot contract them into FMAs: the result is bit-exact
+// against a float32 reference fed the same rows.
+//
+// One warp per token; lane l owns 16-byte vectors l, l+32, ... of the H columns.  For
+// each vector, the K slot rows are loaded together (up to 8 16-byte loads in flight per
+// lane) before the ordered sum.  HBM-bound: N*H*2 + N_shared*H*2 read, T*H*2 written.
+#include "common.cuh"
+
+namespace moe {
+
+enum CombineMode { kWrite = 0, kVerify = 1, kAmax = 2 };
+
+template <int MODE, bool FQ, int KMAX>
+__global__ void __launch_bounds__(256) combine_kernel(
+    const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_map, const float* __restrict__ topk_w, int T,
+    int K, int H, const uint16_t* __restrict__ shared_y, const int32_t* __restrict__ shared_map,
+    const float* __restrict__ fq_scale, uint16_t* __restrict__ out, const uint16_t* __restrict__ expected,
+    int32_t* dev_status, float* amax_out) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = H / 8;
+  const float s = FQ ? *fq_scale : 1.0f;
+  float amax = 0.0f;
+  bool mismatch = false;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+    int my_p = -1;
+    float my_w = 0.0f;
+    if (lane < K) {
+      my_p = inv_map[(size_t)t * K + lane];
+      my_w = topk_w[(size_t)t * K + lane];
+    }
+    const unsigned valid = __ballot_sync(0xffffffffu, lane < K && my_p >= 0);
+    int srow = -1;
+    if (MODE != kAmax && valid && shared_y) srow = shared_map ? shared_map[t] : t;
+    int p[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      p[j] = __shfl_sync(0xffffffffu, my_p, j);
+      w[j] = __shfl_sync(0xffffffffu, my_w, j);
+      if (j >= K) p[j] = -1;
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      uint4 ld[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (p[j] >= 0) ld[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)p[j] * H) + v);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (p[j] < 0) continue;
+        const uint32_t u[4] = {ld[j].x, ld[j].y, ld[j].z, ld[j].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float yv = __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16));
+          float r = __fmul_rn(yv, w[j]);
+          if (MODE == kAmax) {
+            amax = fmaxf(amax, fabsf(r));
+            continue;
+          }
+          if (FQ) r = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(r, s))), s);
+          acc[i] = __fadd_rn(acc[i], r);
+        }
+      }
+      if (MODE == kAmax) continue;
+      if (srow >= 0) {
+        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(shared_y + (size_t)srow * H) + v);
+        const uint32_t u[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          acc[i] = __fadd_rn(acc[i],
+                             __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16)));
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = (uint32_t)f32_to_bf16(acc[2 * i]) | ((uint32_t)f32_to_bf16(acc[2 * i + 1]) << 16);
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      if (MODE == kWrite) {
+        reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = ov;
+      } else {
+        const uint4 ev = __ldg(reinterpret_cast<const uint4*>(expected + (size_t)t * H) + v);
+        mismatch |= (ev.x != ov.x) | (ev.y != ov.y) | (ev.z != ov.z) | (ev.w != ov.w);
+      }
+    }
+  }
+  if (MODE == kVerify) {
+    if (__ballot_sync(0xffffffffu, mismatch) && lane == 0) atomicOr(dev_status, MOE_DEV_VERIFY_MISMATCH);
+  }
+  if (MODE == kAmax) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    // non-negative floats order like their bit patterns as signed ints
+    if (lane == 0 && amax > 0.0f) atomicMax(reinterpret_cast<int*>(amax_out), __float_as_int(amax));
+  }
+}
+
+__global__ void fq_scale_kernel(const float* amax, float* scale) {
+  const float a = *amax;
+  *scale = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
+}
+
+template <int MODE>
+moe_status_t launch_combine(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T, int K, int H,
+                            const uint16_t* shared_y, const int32_t* shared_map, const float* fq_scale,
+                            uint16_t* out, const uint16_t* expected, int32_t* dev_status, float* amax,
+                            cudaStream_t s) {
+  const int blocks = min((T + 7) / 8, num_sms() * 16);
+  const bool fq = fq_scale != nullptr && MODE != kAmax;
+#define MOE_COMBINE_LAUNCH(FQV, KM)                                                                    \
+  combine_kernel<MODE, FQV, KM><<<blocks, 256, 0, s>>>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, \
+                                                       fq_scale, out, expected, dev_status, amax)
+  if (K <= 8) {
+    if (fq) MOE_COMBINE_LAUNCH(true, 8); else MOE_COMBINE_LAUNCH(false, 8);
+  } else {
+    if (fq) MOE_COMBINE_LAUNCH(true, 32); else MOE_COMBINE_LAUNCH(false, 32);
+  }
+#undef MOE_COMBINE_LAUNCH
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+inline moe_status_t check_combine_args(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                                       int K, int H, const uint16_t* shared_y) {
+  if (T < 0 || K < 1 || K > kMaxTopK || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
+  if (T > 0 && (!y || !inv_map || !topk_w)) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(shared_y)) & 15) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_combine(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T, int K,
+                                    int H, const uint16_t* shared_y, const int32_t* shared_map,
+                                    const float* fq_scale, uint16_t* out, void* stream) {
+  using namespace moe;
+  moe_status_t st = check_combine_args(y, inv_map, topk_w, T, K, H, shared_y);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 15)) return MOE_ERR_ARG;
+  return launch_combine<kWrite>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, fq_scale, out, nullptr,
+                                nullptr, nullptr, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_combine_verify(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                                           int K, int H, const uint16_t* shared_y, const int32_t* shared_map,
+                                           const float* fq_scale, const uint16_t* expected, int32_t* dev_status,
+                                           void* stream) {
+  using namespace moe;
+  moe_status_t st = check_combine_args(y, inv_map, topk_w, T, K, H, shared_y);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!expected || !dev_status || (reinterpret_cast<uintptr_t>(expected) & 15)) return MOE_ERR_ARG;
+  return launch_combine<kVerify>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, fq_scale, nullptr, expected,
+                                 dev_status, nullptr, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_combine_amax(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                                         int K, int H, float* amax, void* stream) {
+  using namespace moe;
+  moe_status_t st = check_combine_args(y, inv_map, topk_w, T, K, H, nullptr);
+  if (st != MOE_OK) return st;
+  if (!amax) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  return launch_combine<kAmax>(y, inv_map, topk_w, T, K, H, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                               amax, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_fq_scale_from_amax(const float* amax, float* scale, void* stream) {
+  using namespace moe;
+  if (!amax || !scale) return MOE_ERR_ARG;
+  fq_scale_kernel<<<1, 1, 0, as_stream(stream)>>>(amax, scale);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}

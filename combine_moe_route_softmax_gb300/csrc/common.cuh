@@ -1,0 +1,60 @@
+// Shared device/host helpers of libmoe (sm_103a).  Internal header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+#define MOE_CHECK_LAUNCH()                                   \
+  do {                                                       \
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+inline int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+// E4M3 (e4m3fn) round-to-nearest-even with saturation to +-448 (hardware cvt).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float f) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q), __NV_E4M3);
+  return __half2float(__half(h));
+}
+// 1xN block scale rule: s = amax / 448 (IEEE float32 division), 1 if not positive.
+__device__ __forceinline__ float block_scale(float amax) {
+  float s = __fdiv_rn(amax, 448.0f);
+  return s > 0.0f ? s : 1.0f;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace moe

@@ -1,0 +1,630 @@
+// Grouped GEMM over the expert segments on the 5th-generation tensor cores (sm_103a):
+// tcgen05.mma with accumulators in tensor memory (TMEM), operands staged in shared memory
+// by TMA (cp.async.bulk.tensor, 128-byte swizzle, no multicast), and a persistent
+// per-expert tile scheduler that builds its tile list on the device from cu_seqlens, so
+// the host never needs the segment lengths (no host sync; graph-capturable).
+//
+// MoonEP page: the experts run as three grouped matmuls (gate, up, down) over the
+// cu_seqlens segments, and empty segments simply produce no tiles.  DeepEP page: gate and
+// up are one fused weight with 2n rows; FP8 weights carry block_n x block_k scales.
+//
+// Tile: BM = 128 rows x BN = 256 weight rows x 128 bytes of K per pipeline stage
+// (64 BF16 or 128 E4M3 elements), 4 stages (48 KB each).  For SwiGLU the 256 weight rows
+// of a tile are 128 gate rows and the matching 128 up rows, so one MMA with N = 256
+// yields g and u for 128 output columns side by side in TMEM.
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (its subpartition) and
+//               half (w-2)/4 of the tile's columns.
+// TMEM: 512 columns = two 256-column accumulator buffers, so the epilogue of one
+// accumulation round overlaps the MMAs of the next.
+//   BF16: one round per tile; the whole K loop accumulates in TMEM.
+//   E4M3: one round per 128-wide K block: each block's partial product is scaled by its
+//         activation scale (per row) and weight scale (per 128x128 block) and added into
+//         float32 registers by the epilogue warps ("promotion"), since the scales are
+//         float32 per 128 elements rather than a format the MMA applies itself.
+//
+// Every mbarrier wait is bounded (about 2 s of globaltimer); on expiry the CTA sets
+// MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producer
+// waits (bounded) for its copies in flight, the MMA lane waits (bounded) for its MMAs,
+// and the TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int KB_BYTES = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * KB_BYTES;
+constexpr int B_BYTES = BN * KB_BYTES;
+constexpr int B_HALF = B_BYTES / 2;
+constexpr int STAGE_TX = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_SEG = kMaxExperts + 1;
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+
+struct SmemLayout {
+  static constexpr int a = 0;
+  static constexpr int b = a + STAGES * A_BYTES;
+  static constexpr int bars = b + STAGES * B_BYTES;          // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int n_bars = 2 * STAGES + 5;
+  static constexpr int tmem_slot = bars + n_bars * 8;
+  static constexpr int abort_flag = tmem_slot + 4;
+  static constexpr int xch = abort_flag + 12;                 // float [2][128], 16-aligned
+  static constexpr int cu = xch + 2 * 128 * 4;                // int [MAX_SEG + 1]
+  static constexpr int prefix = cu + (MAX_SEG + 1) * 4;       // int [MAX_SEG + 1]
+  static constexpr int end = prefix + (MAX_SEG + 1) * 4;
+};
+constexpr size_t SMEM_BYTES = SmemLayout::end + 1024;           // + alignment slack
+
+struct Args {
+  const int32_t* cu;
+  int nseg;
+  int rows_cap;
+  int k_dim;
+  int n_dim;
+  int num_w;
+  const float* a_scales;
+  const float* w_scales;
+  const float* wx_scales;
+  void* out;
+  float* out_scales;
+  int32_t* dev_status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false if the pipeline was aborted (by this wait timing out or another role).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > TIMEOUT_NS) {
+      *abort_flag = 1;
+      if (dev_status) atomicOr(dev_status, MOE_DEV_PIPELINE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > TIMEOUT_NS) return;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+template <bool FP8>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  }
+}
+// 32 consecutive float32 columns of this warp's 32 TMEM lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
+// 8-row groups 1024 bytes apart (stride byte offset), start address in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused with 128B swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;             // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: D float32, A/B K-major, N = BN, M = BM; A/B BF16 or E4M3.
+template <bool FP8>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+struct Unit {
+  int seg, row0, row_end, nt;
+};
+__device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, const int* prefix, int nseg) {
+  Unit w;
+  const int mt = u / n_tiles;
+  w.nt = u - mt * n_tiles;
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= mt)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  w.seg = lo;
+  w.row0 = cu[lo] + (mt - prefix[lo]) * BM;
+  w.row_end = cu[lo + 1];
+  return w;
+}
+
+// ------------------------------------------------------------------------ kernel
+template <bool FP8, bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmBx, const Args args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars);
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::tmem_slot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::abort_flag);
+  float* xch = reinterpret_cast<float*>(smem + SmemLayout::xch);
+  int* cu_s = reinterpret_cast<int*>(smem + SmemLayout::cu);
+  int* prefix = reinterpret_cast<int*>(smem + SmemLayout::prefix);
+
+  const int nseg = args.nseg;
+  for (int i = tid; i <= nseg; i += THREADS) cu_s[i] = args.cu[i];
+  if (tid == 64) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), EPI_WARPS);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  // per-segment M-tile counts -> exclusive prefix (warp 0)
+  if (warp == 0) {
+    const int chunk = (nseg + 31) / 32;
+    const int s0 = min(nseg, lane * chunk), s1 = min(nseg, s0 + chunk);
+    int local = 0;
+    for (int s = s0; s < s1; ++s) local += (max(0, cu_s[s + 1] - cu_s[s]) + BM - 1) / BM;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int s = s0; s < s1; ++s) {
+      prefix[s] = run;
+      run += (max(0, cu_s[s + 1] - cu_s[s]) + BM - 1) / BM;
+    }
+    if (lane == 31) prefix[nseg] = incl;
+  }
+  __syncthreads();
+  const int n_tiles = SWIGLU ? (args.n_dim / 2) / 128 : (args.n_dim + BN - 1) / BN;
+  const int total_units = prefix[nseg] * n_tiles;
+  if (static_cast<int>(blockIdx.x) >= total_units) return;  // no work: nothing allocated yet
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  constexpr int KE = FP8 ? 128 : 64;  // K elements per stage
+  const int kblocks = args.k_dim / KE;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s has been armed at least once
+      uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg);
+        const bool extra = w.seg >= args.num_w;
+        const CUtensorMap* mb = extra ? &tmBx : &tmB;
+        const int wbase = extra ? 0 : w.seg * args.n_dim;
+        const int rA = SWIGLU ? wbase + w.nt * 128 : wbase + w.nt * BN;
+        const int rB = SWIGLU ? wbase + args.n_dim / 2 + w.nt * 128 : rA + 128;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar_full(stage), STAGE_TX);
+          armed |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
+          const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
+          tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
+          tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
+          tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // wait for the copies this CTA still has in flight before its shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc<FP8>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t tphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const bool round_start = FP8 || kb == 0;
+          if (round_start) {
+            if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
+          const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
+          const uint32_t dt = tmem_base + buf * BN;
+#pragma unroll
+          for (int k = 0; k < KB_BYTES / 32; ++k) {
+            const uint32_t acc = (FP8 ? k : (kb | k)) != 0;
+            tc_mma<FP8>(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, acc);
+          }
+          tc_commit(bar_empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          const bool round_end = FP8 || kb == kblocks - 1;
+          if (round_end) {
+            tc_commit(bar_tfull(buf));
+            if (++buf == 2) {
+              buf = 0;
+              tphase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        tc_commit(bar_drain);  // arrives once every MMA issued so far has completed
+        mbar_drain(bar_drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM subpartition this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns
+    const int r_in_tile = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    const int kbs_total = kblocks;
+    int buf = 0;
+    uint32_t tphase = 0;
+    const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg);
+      const int row = w.row0 + r_in_tile;
+      const bool row_ok = row < w.row_end;
+      // first output column this thread covers and whether that 128-column block exists
+      const int col0 = SWIGLU ? w.nt * 128 + 64 * half : w.nt * BN + 128 * half;
+      const bool cols_ok = col0 < out_cols;
+      float acc[128];
+      if (FP8) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      }
+      const bool extra = w.seg >= args.num_w;
+      int rounds = FP8 ? kbs_total : 1;
+      bool ok = true;
+      for (int rd = 0; rd < rounds; ++rd) {
+        if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_addr + buf * BN;
+        if (FP8) {
+          // promotion of this K block: acc += partial * (s_a[row, kb] * s_w[block, kb])
+          const int kb = rd;
+          const float sa = (row < args.rows_cap) ? args.a_scales[(size_t)row * kbs_total + kb] : 0.0f;
+          const float* wsc = extra ? args.wx_scales : args.w_scales + (size_t)w.seg * (args.n_dim / 128) * kbs_total;
+          float s0, s1;
+          if (SWIGLU) {
+            s0 = wsc[(size_t)w.nt * kbs_total + kb];
+            s1 = wsc[(size_t)(args.n_dim / 256 + w.nt) * kbs_total + kb];
+          } else {
+            const int blk = (w.nt * BN + 128 * half) / 128;
+            s0 = s1 = cols_ok ? wsc[(size_t)blk * kbs_total + kb] : 0.0f;
+          }
+          s0 *= sa;
+          s1 *= sa;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+                                    : 128 * half + 32 * c;
+            uint32_t r[32];
+            tmem_ld32(tb + tcol, r);
+            tmem_wait_ld();
+            const float sc = (SWIGLU && c >= 2) ? s1 : s0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * c + i]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+                                    : 128 * half + 32 * c;
+            uint32_t r[32];
+            tmem_ld32(tb + tcol, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 * c + i] = __uint_as_float(r[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty(buf));
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1;
+        }
+      }
+      if (!ok) break;
+      // ---- tile epilogue from registers
+      if (SWIGLU) {
+        float h[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
+        if (!FP8) {
+          if (row_ok && cols_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              uint32_t o[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                o[j] = (uint32_t)f32_to_bf16(h[8 * v + 2 * j]) | ((uint32_t)f32_to_bf16(h[8 * v + 2 * j + 1]) << 16);
+              dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        } else {
+          // 1x128 block of h = this thread's 64 columns + the partner half's 64
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(h[i]));
+          xch[half * 128 + r_in_tile] = amax;
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          amax = fmaxf(amax, xch[(1 - half) * 128 + r_in_tile]);
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          const float s = block_scale(amax);
+          if (row_ok && cols_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + (size_t)row * out_cols + col0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t o[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) word |= (uint32_t)f32_to_e4m3(__fdiv_rn(h[16 * v + 4 * j + b], s)) << (8 * b);
+                o[j] = word;
+              }
+              dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (half == 0) args.out_scales[(size_t)row * (out_cols / 128) + w.nt] = s;
+          }
+        }
+      } else {
+        if (row_ok && cols_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              o[j] = (uint32_t)f32_to_bf16(acc[8 * v + 2 * j]) | ((uint32_t)f32_to_bf16(acc[8 * v + 2 * j + 1]) << 16);
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+  }
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+}
+
+// ---------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// rows x inner-elements matrix, box = 128 rows x 128 bytes, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t esz = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(KB_BYTES / esz), 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8, bool SWIGLU>
+moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const Args& args,
+                    int grid, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<FP8, SWIGLU>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = true;
+  }
+  kern<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, bx, args);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+}  // namespace gg
+}  // namespace moe
+
+extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                                         int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
+                                         const float* w_scales, int num_w, const void* w_extra,
+                                         const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
+                                         void* out, float* out_scales, int32_t* dev_status, void* stream) {
+  using namespace moe;
+  using namespace moe::gg;
+  const bool fp8 = dtype == MOE_E4M3;
+  const bool swiglu = epilogue == MOE_EPI_SWIGLU;
+  if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
+  if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SWIGLU) return MOE_ERR_ARG;
+  if (num_segments < 0 || num_segments > MAX_SEG || rows_cap < 0 || num_w < 0) return MOE_ERR_ARG;
+  if (num_segments > num_w + (w_extra ? 1 : 0)) return MOE_ERR_ARG;
+  if (k_dim <= 0 || k_dim % 128 != 0 || n_dim <= 0 || n_dim % 128 != 0) return MOE_ERR_ARG;
+  if (swiglu && (n_dim % 256 != 0)) return MOE_ERR_ARG;
+  if (num_segments == 0 || rows_cap == 0) return MOE_OK;
+  if (!a || !cu_seqlens || !out || (num_w > 0 && !w)) return MOE_ERR_ARG;
+  if (fp8 && (!a_scales || (num_w > 0 && !w_scales) || (w_extra && !w_extra_scales))) return MOE_ERR_ARG;
+  if (fp8 && swiglu && !out_scales) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(w_extra) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return MOE_ERR_ARG;
+  if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
+  CUtensorMap ma, mb, mbx;
+  if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
+  const void* wb = num_w > 0 ? w : w_extra;
+  const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
+  if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
+  if (w_extra) {
+    if (!make_map(&mbx, w_extra, fp8, k_dim, n_dim)) return MOE_ERR_CUDA;
+  } else {
+    mbx = mb;
+  }
+  Args args;
+  args.cu = cu_seqlens;
+  args.nseg = num_segments;
+  args.rows_cap = rows_cap;
+  args.k_dim = k_dim;
+  args.n_dim = n_dim;
+  args.num_w = num_w;
+  args.a_scales = a_scales;
+  args.w_scales = w_scales;
+  args.wx_scales = w_extra_scales;
+  args.out = out;
+  args.out_scales = out_scales;
+  args.dev_status = dev_status;
+  // grid: one CTA per SM, never more than the largest possible number of tiles
+  const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
+  const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
+  const int grid = (int)std::min<long long>(num_sms(), max_units);
+  cudaStream_t s = as_stream(stream);
+  if (fp8)
+    return swiglu ? launch<true, true>(ma, mb, mbx, args, grid, s) : launch<true, false>(ma, mb, mbx, args, grid, s);
+  return swiglu ? launch<false, true>(ma, mb, mbx, args, grid, s) : launch<false, false>(ma, mb, mbx, args, grid, s);
+}

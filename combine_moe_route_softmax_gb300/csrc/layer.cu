@@ -1,0 +1,117 @@
+// The whole MoE layer on one stream with no host synchronisation (so it can be captured
+// in a CUDA graph, the constraint the Mega-MoE page puts on its combine after the first
+// check): route -> permute (+FP8 quantisation) -> grouped GEMM gate/up with fused SwiGLU
+// -> grouped GEMM down -> fixed-order combine.  The shared expert is segment E of both
+// grouped GEMMs and the last slot of the combine.
+//
+// Workspace (caller-owned, sized from the layer's actual shape -- the permute-scratch
+// page's rule -- every region 256-byte aligned):
+//   cu_seqlens [E+2] | src_row [cap] | inv_map [T*K] | shared_map [T] | permute scratch |
+//   xp [cap, H] (+ scales [cap, H/128]) | hs [cap, I] (+ scales [cap, I/128]) | y [cap, H] bf16
+// with cap = T*K + (has_shared ? T : 0).
+#include "common.cuh"
+
+namespace moe {
+
+struct LayerPlan {
+  size_t off_cu, off_src, off_inv, off_smap, off_scratch, off_xp, off_xps, off_hs, off_hss, off_y, total;
+  size_t scratch_bytes;
+  int cap, nseg;
+};
+
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
+  if (!d) return false;
+  if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E < 1 || d->E > kMaxExperts || d->K < 1 || d->K > d->E ||
+      d->K > kMaxTopK || d->H % 128 || d->I % 128 || (d->has_shared != 0 && d->has_shared != 1) ||
+      (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
+    return false;
+  const size_t T = d->T, K = d->K, H = d->H, I = d->I;
+  const size_t cap = T * K + (d->has_shared ? T : 0);
+  if (cap > 0x7fffffffull) return false;
+  const size_t esz = d->dtype == MOE_E4M3 ? 1 : 2;
+  const bool fp8 = d->dtype == MOE_E4M3;
+  p->cap = (int)cap;
+  p->nseg = d->E + d->has_shared;
+  p->scratch_bytes = moe_permute_workspace_bytes(d->T, d->K, d->E, d->has_shared);
+  size_t o = 0;
+  p->off_cu = o;      o = align256(o + 4 * (size_t)(p->nseg + 1));
+  p->off_src = o;     o = align256(o + 4 * cap);
+  p->off_inv = o;     o = align256(o + 4 * T * K);
+  p->off_smap = o;    o = align256(o + 4 * T);
+  p->off_scratch = o; o = align256(o + p->scratch_bytes);
+  p->off_xp = o;      o = align256(o + cap * H * esz);
+  p->off_xps = o;     o = align256(o + (fp8 ? cap * (H / 128) * 4 : 0));
+  p->off_hs = o;      o = align256(o + cap * I * esz);
+  p->off_hss = o;     o = align256(o + (fp8 ? cap * (I / 128) * 4 : 0));
+  p->off_y = o;       o = align256(o + cap * H * 2);
+  p->total = o;
+  return true;
+}
+
+}  // namespace moe
+
+extern "C" size_t moe_layer_workspace_bytes(const moe_layer_desc_t* d) {
+  moe::LayerPlan p;
+  return moe::plan_layer(d, &p) ? p.total : 0;
+}
+
+extern "C" moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe_layer_views_t* v) {
+  moe::LayerPlan p;
+  if (!moe::plan_layer(d, &p) || !ws || !v) return MOE_ERR_ARG;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const bool fp8 = d->dtype == MOE_E4M3;
+  v->cu_seqlens = reinterpret_cast<int32_t*>(b + p.off_cu);
+  v->src_row = reinterpret_cast<int32_t*>(b + p.off_src);
+  v->inv_map = reinterpret_cast<int32_t*>(b + p.off_inv);
+  v->shared_map = d->has_shared ? reinterpret_cast<int32_t*>(b + p.off_smap) : nullptr;
+  v->xp = b + p.off_xp;
+  v->xp_scales = fp8 ? reinterpret_cast<float*>(b + p.off_xps) : nullptr;
+  v->hs = b + p.off_hs;
+  v->hs_scales = fp8 ? reinterpret_cast<float*>(b + p.off_hss) : nullptr;
+  v->y = reinterpret_cast<uint16_t*>(b + p.off_y);
+  v->cap = p.cap;
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_layer_weights_t* w,
+                                          const float* logits, const int32_t* num_tokens, int32_t* topk_idx,
+                                          float* topk_w, const uint16_t* x, const float* fq_scale, uint16_t* out,
+                                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  using namespace moe;
+  LayerPlan p;
+  if (!plan_layer(d, &p) || !w) return MOE_ERR_ARG;
+  if (!ws || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return MOE_ERR_ARG;
+  if (d->T == 0) return MOE_OK;
+  if (!topk_idx || !topk_w || !x || !out || !w->w13 || !w->w2) return MOE_ERR_ARG;
+  const bool fp8 = d->dtype == MOE_E4M3;
+  if (fp8 && (!w->w13_scales || !w->w2_scales)) return MOE_ERR_ARG;
+  if (d->has_shared && (!w->shared_w13 || !w->shared_w2 ||
+                        (fp8 && (!w->shared_w13_scales || !w->shared_w2_scales))))
+    return MOE_ERR_ARG;
+  moe_layer_views_t v;
+  moe_layer_views(d, ws, &v);
+  moe_status_t st;
+  if (logits) {
+    st = moe_route_topk(logits, d->T, d->E, d->K, num_tokens, topk_idx, topk_w, stream);
+    if (st != MOE_OK) return st;
+  }
+  st = moe_permute(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, v.cu_seqlens,
+                   v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes,
+                   dev_status, stream);
+  if (st != MOE_OK) return st;
+  const void* sx13 = d->has_shared ? w->shared_w13 : nullptr;
+  const void* sx2 = d->has_shared ? w->shared_w2 : nullptr;
+  st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
+                        sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
+                        v.hs_scales, dev_status, stream);
+  if (st != MOE_OK) return st;
+  st = moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, w->w2_scales, d->E, sx2,
+                        d->has_shared ? w->shared_w2_scales : nullptr, d->dtype, MOE_EPI_NONE, v.y, nullptr,
+                        dev_status, stream);
+  if (st != MOE_OK) return st;
+  return moe_combine(v.y, v.inv_map, topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr, v.shared_map,
+                     fq_scale, out, stream);
+}

@@ -1,0 +1,354 @@
+// Permute (dispatch into the expert-major layout): stable counting sort of the valid
+// (token, slot) pairs by expert id, then a gather of each row's token activations.
+//
+// MoonEP page: dispatch returns the rows "already grouped per expert row" ([NvS, H]) plus
+// cu_seqlens, and the experts run as a grouped GEMM over those segments.  Permute-scratch
+// page: the scratch is sized from the inputs actually received and holds index metadata
+// only.  DeepEP page: the low-latency dispatch takes BF16 tokens and, for FP8, quantises
+// them internally and sends "tokens, and scales" -- here the 1x128 quantisation is fused
+// into the row gather.
+//
+// Four launches, none of which waits on another block:
+//   count   per-block per-segment histograms             (reads T*K*4 B)
+//   scan    one block: per-segment exclusive prefix over blocks + cu_seqlens
+//   scatter per-block: per-warp histograms, a warp-level scan, then an ordered walk with
+//           __match_any_sync ranks -> src_row / inv_map / shared_map (stable by slot)
+//   gather  Xp[p] = x[token(p)] with 16-byte vector loads/stores, one warp per row
+//           (BF16 copy, or E4M3 codes + 1x128 scales).  HBM-bound:
+//           T_valid*H*2 read + N*H*(2 | 1 + 4/128) written.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kChunkTok = 64;                 // tokens per count/scatter block
+constexpr int kTokPerWarp = kChunkTok / kPermWarps;
+
+__device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
+
+__global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32_t* __restrict__ idx, int T,
+                                                                     int K, int E, int with_shared,
+                                                                     int32_t* __restrict__ counts,
+                                                                     int32_t* dev_status) {
+  extern __shared__ int hist[];
+  const int nseg = E + with_shared;
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kChunkTok;
+  const int t1 = min(T, t0 + kChunkTok);
+  bool bad = false;
+  for (int s = t0 * K + threadIdx.x; s < t1 * K; s += blockDim.x) {
+    const int e = idx[s];
+    if (valid_id(e, E))
+      atomicAdd(&hist[e], 1);
+    else if (e != -1)
+      bad = true;
+  }
+  if (with_shared) {
+    for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+      bool any = false;
+      for (int k = 0; k < K; ++k) any |= valid_id(idx[(size_t)t * K + k], E);
+      if (any) atomicAdd(&hist[E], 1);
+    }
+  }
+  if (bad && dev_status) atomicOr(dev_status, MOE_DEV_BAD_EXPERT);
+  __syncthreads();
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) counts[(size_t)blockIdx.x * nseg + i] = hist[i];
+}
+
+// One block of 1024 threads.  counts[b][e] -> global row offset of block b's rows of
+// segment e; cu_seqlens = exclusive prefix of the per-segment totals.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ counts, int nblk, int nseg,
+                                                            int32_t* __restrict__ cu_seqlens) {
+  __shared__ int tot[2 * 1024];
+  __shared__ int warp_sums[32];
+  for (int e = threadIdx.x; e < 2 * 1024; e += blockDim.x) tot[e] = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int c = counts[(size_t)b * nseg + e];
+      counts[(size_t)b * nseg + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of tot[0 .. 2048): thread i owns elements 2i, 2i+1
+  const int i = threadIdx.x;
+  const int a0 = tot[2 * i], a1 = tot[2 * i + 1];
+  int incl = a0 + a1;
+  const int lane = i & 31, warp = i >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws += v;
+    }
+    warp_sums[lane] = ws;  // inclusive
+  }
+  __syncthreads();
+  const int excl = incl - (a0 + a1) + (warp > 0 ? warp_sums[warp - 1] : 0);
+  __syncthreads();
+  tot[2 * i] = excl;
+  tot[2 * i + 1] = excl + a0;
+  __syncthreads();
+  for (int e = threadIdx.x; e <= nseg; e += blockDim.x) cu_seqlens[e] = tot[e];
+  for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
+    const int base = tot[e];
+    for (int b = 0; b < nblk; ++b) counts[(size_t)b * nseg + e] += base;
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
+    const int32_t* __restrict__ idx, int T, int K, int E, int with_shared, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ cu_seqlens, int cap, int32_t* __restrict__ src_row, int32_t* __restrict__ inv_map,
+    int32_t* __restrict__ shared_map) {
+  extern __shared__ int whist[];  // [kPermWarps][nseg]
+  const int nseg = E + with_shared;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kPermWarps * nseg; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kChunkTok;
+  const int wt0 = min(T, t0 + warp * kTokPerWarp);
+  const int wt1 = min(T, wt0 + kTokPerWarp);
+  const int ws0 = wt0 * K, ws1 = wt1 * K;
+  int* my = whist + warp * nseg;
+  // 1. per-warp histogram
+  for (int s = ws0 + lane; s < ws1; s += 32) {
+    const int e = idx[s];
+    if (valid_id(e, E)) atomicAdd(&my[e], 1);
+  }
+  if (with_shared) {
+    for (int t = wt0 + lane; t < wt1; t += 32) {
+      bool any = false;
+      for (int k = 0; k < K; ++k) any |= valid_id(idx[(size_t)t * K + k], E);
+      if (any) atomicAdd(&my[E], 1);
+    }
+  }
+  __syncthreads();
+  // 2. each warp's starting row per segment = block offset + earlier warps' counts
+  for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
+    int run = offsets[(size_t)blockIdx.x * nseg + e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = whist[w * nseg + e];
+      whist[w * nseg + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3. ordered walk: lanes holding the same expert rank themselves by lane order
+  for (int base = ws0; base < ws1; base += 32) {
+    const int s = base + lane;
+    const bool inr = s < ws1;
+    const int e = inr ? idx[s] : -1;
+    const bool ok = inr && valid_id(e, E);
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+    int rank = 0;
+    if (ok) {
+      rank = __popc(peers & lanemask_lt());
+      const int pos = my[e] + rank;
+      src_row[pos] = s;
+      inv_map[s] = pos;
+    } else if (inr) {
+      inv_map[s] = -1;
+    }
+    __syncwarp();
+    if (ok && rank == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (with_shared) {
+    for (int tb = wt0; tb < wt1; tb += 32) {
+      const int t = tb + lane;
+      const bool inr = t < wt1;
+      bool any = false;
+      if (inr)
+        for (int k = 0; k < K; ++k) any |= valid_id(idx[(size_t)t * K + k], E);
+      const unsigned ball = __ballot_sync(0xffffffffu, any);
+      if (any) {
+        const int pos = my[E] + __popc(ball & lanemask_lt());
+        src_row[pos] = T * K + t;
+        shared_map[t] = pos;
+      } else if (inr) {
+        shared_map[t] = -1;
+      }
+      __syncwarp();
+      if (lane == 0) my[E] += __popc(ball);
+      __syncwarp();
+    }
+  }
+  // rows past the last one: -1
+  const int total = cu_seqlens[nseg];
+  for (int p = total + blockIdx.x * blockDim.x + threadIdx.x; p < cap; p += gridDim.x * blockDim.x)
+    src_row[p] = -1;
+}
+
+__device__ __forceinline__ int row_token(int src, int TK, int K) { return src < TK ? src / K : src - TK; }
+
+__global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t* __restrict__ x, int T, int K,
+                                                                  int H, const int32_t* __restrict__ src_row,
+                                                                  const int32_t* __restrict__ cu_seqlens,
+                                                                  int nseg, uint16_t* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int total = cu_seqlens[nseg];
+  const int nvec = H / 8;
+  for (int p = gw; p < total; p += nw) {
+    const int t = row_token(src_row[p], T * K, K);
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* o = reinterpret_cast<uint4*>(xp + (size_t)p * H);
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 a = __ldg(in + v), b = __ldg(in + v + 32), c = __ldg(in + v + 64), d = __ldg(in + v + 96);
+      o[v] = a;
+      o[v + 32] = b;
+      o[v + 64] = c;
+      o[v + 96] = d;
+    }
+    for (; v < nvec; v += 32) o[v] = __ldg(in + v);
+  }
+}
+
+// One 1x128 block per half-warp: lane l of a half-warp converts elements [8l, 8l+8).
+__device__ __forceinline__ void quant_row_1x128(const uint16_t* __restrict__ in, uint8_t* __restrict__ q,
+                                                float* __restrict__ scales, int H, int lane) {
+  const int nvec = H / 8;
+  for (int v0 = 0; v0 < nvec; v0 += 32) {
+    const int v = v0 + lane;
+    const bool live = v < nvec;
+    float f[8];
+    float amax = 0.0f;
+    if (live) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(in) + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (live) {
+      const float s = block_scale(amax);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
+      reinterpret_cast<uint2*>(q)[v] = make_uint2(lo, hi);
+      if ((lane & 15) == 0) scales[v / 16] = s;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) permute_gather_e4m3_kernel(const uint16_t* __restrict__ x, int T, int K,
+                                                                  int H, const int32_t* __restrict__ src_row,
+                                                                  const int32_t* __restrict__ cu_seqlens,
+                                                                  int nseg, uint8_t* __restrict__ xp,
+                                                                  float* __restrict__ xp_scales) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int total = cu_seqlens[nseg];
+  for (int p = gw; p < total; p += nw) {
+    const int t = row_token(src_row[p], T * K, K);
+    quant_row_1x128(x + (size_t)t * H, xp + (size_t)p * H, xp_scales + (size_t)p * (H / 128), H, lane);
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int rows, int cols,
+                                                        uint8_t* __restrict__ q, float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < rows; r += nw)
+    quant_row_1x128(x + (size_t)r * cols, q + (size_t)r * cols, scales + (size_t)r * (cols / 128), cols, lane);
+}
+
+inline int perm_blocks(int T) { return (T + kChunkTok - 1) / kChunkTok; }
+
+}  // namespace moe
+
+extern "C" size_t moe_permute_workspace_bytes(int T, int K, int E, int with_shared) {
+  using namespace moe;
+  if (T < 0 || K < 1 || E < 1 || E > kMaxExperts) return 0;
+  const size_t nseg = (size_t)E + (with_shared ? 1 : 0);
+  const size_t bytes = (size_t)perm_blocks(T) * nseg * sizeof(int32_t);
+  return ((bytes + 255) / 256) * 256 + 256;
+}
+
+extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                    const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp,
+                                    float* xp_scales, int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
+                                    int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    void* stream) {
+  using namespace moe;
+  if (T < 0 || K < 1 || K > kMaxTopK || E < 1 || E > kMaxExperts || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
+  if (with_shared != 0 && with_shared != 1) return MOE_ERR_ARG;
+  if (out_dtype != MOE_BF16 && out_dtype != MOE_E4M3) return MOE_ERR_ARG;
+  if (!cu_seqlens) return MOE_ERR_ARG;
+  const int nseg = E + with_shared;
+  cudaStream_t s = as_stream(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(cu_seqlens, 0, sizeof(int32_t) * (nseg + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (!topk_idx || !x || !xp || !src_row || !inv_map || (with_shared && !shared_map)) return MOE_ERR_ARG;
+  if (out_dtype == MOE_E4M3 && !xp_scales) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xp)) & 15) return MOE_ERR_ARG;
+  if ((size_t)T * K + T > 0x7fffffffull) return MOE_ERR_ARG;
+  const size_t need = moe_permute_workspace_bytes(T, K, E, with_shared);
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  int32_t* counts = static_cast<int32_t*>(ws);
+  const int nblk = perm_blocks(T);
+  const int cap = T * K + (with_shared ? T : 0);
+  permute_count_kernel<<<nblk, kPermThreads, nseg * sizeof(int), s>>>(topk_idx, T, K, E, with_shared, counts,
+                                                                        dev_status);
+  MOE_CHECK_LAUNCH();
+  permute_scan_kernel<<<1, 1024, 0, s>>>(counts, nblk, nseg, cu_seqlens);
+  MOE_CHECK_LAUNCH();
+  const size_t scatter_smem = (size_t)kPermWarps * nseg * sizeof(int);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    attr_set = true;
+  }
+  permute_scatter_kernel<<<nblk, kPermThreads, scatter_smem, s>>>(topk_idx, T, K, E, with_shared, counts,
+                                                                  cu_seqlens, cap, src_row, inv_map, shared_map);
+  MOE_CHECK_LAUNCH();
+  const int gblocks = num_sms() * 8;
+  if (out_dtype == MOE_BF16)
+    permute_gather_bf16_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, src_row, cu_seqlens, nseg,
+                                                       static_cast<uint16_t*>(xp));
+  else
+    permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, src_row, cu_seqlens, nseg,
+                                                       static_cast<uint8_t*>(xp), xp_scales);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,
+                                             void* stream) {
+  using namespace moe;
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !scales) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
+  const int blocks = min((rows + 7) / 8, num_sms() * 8);
+  quant_act_kernel<<<blocks, 256, 0, as_stream(stream)>>>(x, rows, cols, q, scales);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}

@@ -1,0 +1,260 @@
+/*
+ * moe.h -- C ABI of libmoe: the single-GPU Mixture-of-Experts layer hot path on GB300
+ * (sm_103a): route -> permute -> grouped GEMM (gate/up + SwiGLU, down) -> combine.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named in a signature are DEVICE pointers unless the comment says "host".
+ *   All buffers are owned by the caller; the library never allocates, frees, copies to
+ *   the host or synchronises.  Every call only enqueues kernels on `stream` (a
+ *   cudaStream_t passed as void*; NULL = the legacy default stream) and returns, so a
+ *   sequence of calls can be captured in a CUDA graph.
+ * - Host-side argument errors (bad sizes, null required pointers, a workspace that is
+ *   too small) are detected before anything is enqueued and returned as a moe_status_t;
+ *   nothing is launched in that case.  MOE_ERR_CUDA reports a failed launch.
+ * - Data errors found on the device (an expert id outside [-1, E), a verification
+ *   mismatch, a pipeline wait that ran out of time) never trap: they OR a bit into the
+ *   caller's int32 `dev_status` word (device memory, zeroed by the caller, sticky).
+ * - Tensors are dense and row-major.  BF16 is passed as uint16_t bit patterns, FP8 E4M3
+ *   ("e4m3fn": bias 7, max 448, no infinities) as uint8_t codes.
+ * - T tokens (rows of the batch, possibly a padded bucket), H hidden size, I expert
+ *   intermediate size, E routed experts, K experts per token.  H and I must be
+ *   multiples of 128 (the 128-wide tile constraint the MoonEP page validates at layout
+ *   construction), 1 <= K <= min(E, 32), E <= 1024.
+ *
+ * Sources (four pull-request pages):
+ *   [MegaMoE]  "Add MoE dispatch/combine fake quantization for vLLM's DeepGEMM Mega-MoE"
+ *   [DeepEP]   "[Kernel] DeepEP dispatch-combine kernel integration"
+ *   [MoonEP]   "[Distributed][MoonEP] BF16 integration of MoonEP balanced EP backend"
+ *   [Scratch]  "[Bugfix][MoE] Size the permute scratch from its inputs"
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,          /* bad size or null required pointer (host-side, nothing launched) */
+  MOE_ERR_WORKSPACE = 2,    /* workspace smaller than the size query returns */
+  MOE_ERR_UNSUPPORTED = 3,  /* valid request this build does not implement */
+  MOE_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_E4M3 = 1 } moe_dtype_t;
+typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
+
+/* Bits of the device status word. */
+#define MOE_DEV_BAD_EXPERT 1        /* an expert id outside [-1, E): slot treated as padding */
+#define MOE_DEV_VERIFY_MISMATCH 2   /* moe_combine_verify found an element that differs */
+#define MOE_DEV_PIPELINE_TIMEOUT 4  /* a GEMM pipeline wait gave up; its output is invalid */
+
+/* Version of this ABI (bumped on any signature change). */
+int moe_abi_version(void);
+/* Static, human-readable name of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+/* ---------------------------------------------------------------------------- route
+ * Router: softmax over E, top-K, renormalise over the K chosen.
+ * [DeepEP] carries per-token topk_weights / topk_ids into dispatch and [MoonEP] speaks
+ * of "[T, K] IDs"; neither page spells out the router, so this is the plain
+ * softmax -> top-k -> renormalise reading.
+ *   logits     float32 [T, E], finite.
+ *   num_tokens nullable device int32 scalar n: rows t >= n are padding of a receive
+ *              bucket ([Scratch]: power-of-two buckets) and get ids -1, weights 0.  NULL
+ *              means all T rows are tokens.  Read on the device, so a captured graph can
+ *              be replayed with a different n.
+ *   topk_idx   out int32 [T, K]: expert ids in descending logit order, ties to the lower
+ *              id (bit-exact: chosen on the float32 logits).
+ *   topk_w     out float32 [T, K]: w_k = e^{l_k - l_0} / sum_j e^{l_j - l_0}, computed in
+ *              float32 with expf (the full softmax denominator cancels).
+ * Errors: MOE_ERR_ARG if T < 0, E < 1 or E > 1024, K < 1, K > min(E, 32), a null
+ * pointer with T > 0. */
+moe_status_t moe_route_topk(const float* logits, int T, int E, int K, const int32_t* num_tokens,
+                            int32_t* topk_idx, float* topk_w, void* stream);
+
+/* -------------------------------------------------------------------------- permute
+ * Dispatch into the expert-major layout: a stable counting sort of the valid
+ * (token, slot) pairs by expert id ([MoonEP]: rows "already grouped per expert row",
+ * [NvS, H] plus cu_seqlens; [DeepEP]: moe_permute_unpermute), then a gather of each
+ * row's token.  Flat slot s = t*K + k; segment e holds the slots with topk_idx == e in
+ * ascending s.  topk_idx == -1 marks padding ([MegaMoE]: valid = topk_idx >= 0): no row.
+ *
+ * with_shared = 1 appends segment E for the shared expert: every token with at least
+ * one valid slot, ascending t, source index T*K + t ([MegaMoE]: the fused shared
+ * expert's slot; here it is one more dense segment of the same grouped GEMM).
+ *
+ * Sizes come from the inputs, never from a model config ([Scratch]: the bound is the
+ * rows times experts_per_token actually received):
+ *   cap = T*K + (with_shared ? T : 0)   rows of xp / src_row
+ *   nseg = E + with_shared              segments
+ *   x          BF16 [T, H] token activations.
+ *   out_dtype  MOE_BF16: xp is BF16 [cap, H], exact copies of the rows.
+ *              MOE_E4M3: xp is E4M3 [cap, H] and xp_scales float32 [cap, H/128]: each
+ *              row quantised per 1x128 block on the fly (s = amax/448, 1 if amax is 0;
+ *              q = e4m3_rn_satfinite(x / s)), the internal FP8 quantisation the [DeepEP]
+ *              low-latency dispatch applies to BF16 tokens.
+ *   cu_seqlens out int32 [nseg + 1], cu[0] = 0, cu[nseg] = rows written (N).
+ *   src_row    out int32 [cap]: source index of each row (t*K+k, or T*K+t for a shared
+ *              row); -1 for rows >= N.
+ *   inv_map    out int32 [T, K]: row of each slot, -1 for padding.
+ *   shared_map out int32 [T] (required iff with_shared): shared row of each token, or -1.
+ *   ws         scratch of at least moe_permute_workspace_bytes(T, K, E, with_shared) bytes,
+ *              256-byte aligned; index metadata only ([Scratch]: the scratch "holds only
+ *              index metadata"), no state kept between calls.
+ *   dev_status nullable; MOE_DEV_BAD_EXPERT is ORed in for ids outside [-1, E).
+ * Rows of xp at or past N are not written.
+ * Errors: MOE_ERR_ARG for bad sizes / null pointers, MOE_ERR_WORKSPACE if ws_bytes is short. */
+size_t moe_permute_workspace_bytes(int T, int K, int E, int with_shared);
+moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                         const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp, float* xp_scales,
+                         int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map, int32_t* shared_map,
+                         void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------- FP8 quantise
+ * Activation quantisation per 1x128 block ([DeepEP]: FP8 dispatch of "tokens, and
+ * scales" dequantised at the receiver):  x BF16 [rows, cols] -> q E4M3 [rows, cols],
+ * scales float32 [rows, cols/128]; s = amax/448 (1 if that is not positive),
+ * q = e4m3_rn_satfinite(x / s), divisions in IEEE float32.  cols % 128 == 0. */
+moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,
+                                  void* stream);
+/* Weight quantisation per 128x128 block ([DeepEP] test: block_n x block_k weight tiles):
+ * w BF16 [mats, rows, cols] -> q E4M3 same shape, scales float32
+ * [mats, rows/128, cols/128], same rule as above.  rows % 128 == cols % 128 == 0.
+ * A one-time weight-preparation call (outside the layer). */
+moe_status_t moe_quantize_weight_fp8(const uint16_t* w, int mats, int rows, int cols, uint8_t* q,
+                                     float* scales, void* stream);
+
+/* ---------------------------------------------------------------------- grouped GEMM
+ * Grouped GEMM over the cu_seqlens segments ([MoonEP]: the experts are grouped GEMMs,
+ * gate, up and down, "over the cu_seqlens segments"; "empty segments ... are skipped").
+ * For each segment s and each row r in [cu[s], cu[s+1]):
+ *     acc[r, n] = sum_k a[r, k] * W_s[n, k]      (FP32 accumulation, tensor cores)
+ * W_s = w + s*n_dim*k_dim for s < num_w, and w_extra for s == num_w (the shared expert).
+ *   a          BF16 or E4M3 [rows_cap, k_dim]; a_scales float32 [rows_cap, k_dim/128] for E4M3.
+ *   w          [num_w, n_dim, k_dim] (K-major rows) of dtype; w_scales float32
+ *              [num_w, n_dim/128, k_dim/128] for E4M3 (dequantised value = q * s).
+ *   w_extra    nullable [n_dim, k_dim]; w_extra_scales [n_dim/128, k_dim/128] for E4M3.
+ *   epilogue   MOE_EPI_NONE:   out BF16 [rows_cap, n_dim] = bf16_rn(acc).
+ *              MOE_EPI_SWIGLU: n_dim = 2*I, weight rows [0, I) are the gate and [I, 2I) the
+ *              up projection ([DeepEP]: w1 with 2n rows); h = silu(g) * u with
+ *              silu(z) = z / (1 + e^-z), out [rows_cap, I] = bf16_rn(h) for BF16, or
+ *              E4M3 codes with out_scales float32 [rows_cap, I/128] (1x128 blocks, the
+ *              rule of moe_quantize_act_fp8) for E4M3.
+ *   num_segments <= num_w + (w_extra != NULL).  Rows of out outside every segment are not
+ *   written.  k_dim % 128 == 0, n_dim % 128 == 0 (SwiGLU: I % 128 == 0).
+ *   dev_status nullable; MOE_DEV_PIPELINE_TIMEOUT if a pipeline wait gave up.
+ * Errors: MOE_ERR_ARG for bad sizes / null pointers / misaligned pointers (a, w and out
+ * must be 16-byte aligned). */
+moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                              int num_segments, int rows_cap, int k_dim, int n_dim,
+                              const void* w, const float* w_scales, int num_w,
+                              const void* w_extra, const float* w_extra_scales,
+                              moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
+                              int32_t* dev_status, void* stream);
+
+/* -------------------------------------------------------------------------- combine
+ * Fixed-order combine ([MegaMoE]: the router-weighted per-(token, top-k slot) rows are
+ * summed "in the kernel's order (ascending slot, FP32 from zero, one BF16 rounding; a
+ * fused shared expert's slot last and unquantized)"):
+ *     acc = +0.0f
+ *     for k = 0..K-1 with inv_map[t,k] >= 0:
+ *         r = float(y[inv_map[t,k]]) * topk_w[t,k]          (float32 product)
+ *         if fq_scale: r = float(e4m3_rn_satfinite(r * s)) / s    (fake-quant, float32)
+ *         acc = acc + r                                     (float32, no FMA)
+ *     if the token has a valid slot and shared_y: acc = acc + float(shared row)
+ *     out[t] = bf16_rn(acc)                   (a token with no valid slot gets +0)
+ *   y          BF16 [rows, H] expert outputs in the permuted layout.
+ *   inv_map    int32 [T, K] from moe_permute (-1 = padding slot, never read).
+ *   topk_w     float32 [T, K].
+ *   shared_y   nullable BF16: the shared expert's rows; row of token t is shared_map[t]
+ *              when shared_map is given (e.g. y itself with moe_permute's shared_map),
+ *              else t.
+ *   fq_scale   nullable device float32 scalar s ([MegaMoE]: a calibrated or constant
+ *              global combine scale; here s = 448 / amax).
+ *   out        BF16 [T, H].
+ * Bit-exact against a float32 reference given the same y rows. */
+moe_status_t moe_combine(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T, int K,
+                         int H, const uint16_t* shared_y, const int32_t* shared_map,
+                         const float* fq_scale, uint16_t* out, void* stream);
+
+/* Layout self-check ([MegaMoE]: "each buffer checks that its rows reproduce the kernel
+ * output bit for bit"; inside a graph the check runs on the device).  Recomputes the
+ * combine from the same arguments and compares it bit for bit with `expected`
+ * (BF16 [T, H]); any difference ORs MOE_DEV_VERIFY_MISMATCH into dev_status (required).
+ * Never asserts or traps. */
+moe_status_t moe_combine_verify(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                                int K, int H, const uint16_t* shared_y, const int32_t* shared_map,
+                                const float* fq_scale, const uint16_t* expected, int32_t* dev_status,
+                                void* stream);
+
+/* Calibration ([MegaMoE]: algorithm "max"; "the calibrated amax equaled the max of what
+ * each quantizer saw"): amax = max(amax, max |float(y[inv_map[t,k]]) * topk_w[t,k]|) over
+ * every valid slot.  amax is a device float32 the caller zeroes first; repeated calls
+ * accumulate (max).  Exact (max is order-independent). */
+moe_status_t moe_combine_amax(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                              int K, int H, float* amax, void* stream);
+/* scale = 448 / amax in float32 (1 if amax is 0), on the device. */
+moe_status_t moe_fq_scale_from_amax(const float* amax, float* scale, void* stream);
+
+/* ---------------------------------------------------------------------------- layer
+ * The whole layer in one call, one stream, no host synchronisation:
+ *   route (if logits) -> permute (+ FP8 quantisation for E4M3) -> grouped GEMM gate/up
+ *   with fused SwiGLU -> grouped GEMM down -> combine.  The shared expert, when present,
+ *   is segment E of both grouped GEMMs (it must have the routed experts' I). */
+typedef struct {
+  int T;              /* rows of the batch (a receive bucket may pad them) */
+  int H, I, E, K;
+  moe_dtype_t dtype;  /* MOE_BF16, or MOE_E4M3 (weights and activations FP8, 128-blocks) */
+  int has_shared;     /* 1: one shared expert, added last in the combine, never quantised */
+} moe_layer_desc_t;
+
+typedef struct {
+  const void* w13;        /* [E, 2I, H] gate rows then up rows, BF16 or E4M3 */
+  const float* w13_scales;/* E4M3 only: [E, 2I/128, H/128] */
+  const void* w2;         /* [E, H, I] */
+  const float* w2_scales; /* E4M3 only: [E, H/128, I/128] */
+  const void* shared_w13; /* has_shared: [2I, H] */
+  const float* shared_w13_scales;
+  const void* shared_w2;  /* has_shared: [H, I] */
+  const float* shared_w2_scales;
+} moe_layer_weights_t;
+
+/* Pointers into a layer workspace, for inspection and calibration (all device). */
+typedef struct {
+  void* xp; float* xp_scales;   /* permuted activations [cap, H] (+ [cap, H/128]) */
+  void* hs; float* hs_scales;   /* SwiGLU output [cap, I] (+ [cap, I/128]) */
+  uint16_t* y;                  /* expert outputs BF16 [cap, H] */
+  int32_t* cu_seqlens;          /* [E + has_shared + 1] */
+  int32_t* src_row;             /* [cap] */
+  int32_t* inv_map;             /* [T, K] */
+  int32_t* shared_map;          /* [T] or NULL */
+  int cap;                      /* T*K + (has_shared ? T : 0) */
+} moe_layer_views_t;
+
+/* Workspace bytes for a layer of this shape (0 for an invalid descriptor). */
+size_t moe_layer_workspace_bytes(const moe_layer_desc_t* d);
+/* Fill `views` (host struct) with the sub-buffers of `ws`. */
+moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe_layer_views_t* views);
+
+/*   d, w       host structs (read during the call only).
+ *   logits     nullable float32 [T, E]: route inside the layer (num_tokens as in
+ *              moe_route_topk) and write topk_idx / topk_w; NULL: topk_idx / topk_w are
+ *              inputs (e.g. routed elsewhere, with padding slots set to -1 by the caller).
+ *   x          BF16 [T, H];  fq_scale nullable device scalar (combine fake-quant);
+ *   out        BF16 [T, H];  ws / ws_bytes: workspace, 256-byte aligned.
+ * Errors: as the step calls; MOE_ERR_WORKSPACE if ws_bytes < moe_layer_workspace_bytes. */
+moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_layer_weights_t* w,
+                               const float* logits, const int32_t* num_tokens, int32_t* topk_idx,
+                               float* topk_w, const uint16_t* x, const float* fq_scale, uint16_t* out,
+                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,67 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every function that
+include/moe.h declares, and its host-only calls (sizes, argument checks) behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_moe_route_softmax_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from combine_moe_route_softmax_gb300 import build
+        build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ("moe_route_topk", "moe_permute", "moe_grouped_gemm", "moe_combine", "moe_layer_forward",
+              "moe_permute_workspace_bytes", "moe_layer_workspace_bytes", "moe_combine_verify"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in moe._SIGS, f"binding has no signature for {name}"
+
+
+def test_host_only_calls(lib):
+    assert lib.moe_abi_version() == 1
+    assert lib.moe_status_string(2) == b"workspace too small"
+    # scratch sized from the inputs: grows with T, K and E
+    a = lib.moe_permute_workspace_bytes(128, 8, 256, 1)
+    b = lib.moe_permute_workspace_bytes(16384, 8, 256, 1)
+    assert 0 < a < b and b % 256 == 0
+    assert lib.moe_permute_workspace_bytes(16, 2, 0, 0) == 0
+
+
+def test_layer_workspace_size(lib):
+    d = moe.LayerDesc(16384, 7168, 2048, 256, 8, moe.MOE_BF16, 1)
+    n = lib.moe_layer_workspace_bytes(ctypes.byref(d))
+    cap = 16384 * 8 + 16384
+    assert n >= cap * 7168 * 2 * 2 + cap * 2048 * 2
+    bad = moe.LayerDesc(16, 100, 2048, 8, 2, moe.MOE_BF16, 0)   # H not a multiple of 128
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_argument_errors_launch_nothing(lib):
+    # K > E, and H % 128 != 0, are rejected on the host before any CUDA call
+    assert lib.moe_route_topk(None, 4, 2, 3, None, None, None, None) == 1
+    assert lib.moe_permute(None, 4, 2, 8, 0, None, 100, 0, None, None, None, None, None, None, None, 0, None,
+                           None) == 1
+    assert lib.moe_grouped_gemm(None, None, None, 1, 16, 100, 256, None, None, 1, None, None, 0, 0, None, None,
+                                None, None) == 1
+    assert lib.moe_combine(None, None, None, 4, 2, 100, None, None, None, None, None) == 1

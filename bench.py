@@ -431,8 +431,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--cpu-tokens", type=int, default=8)
-    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -3,12 +3,13 @@
 // float32 in ascending slot order starting from +0, add the shared expert's row last and
 // unquantised, round once to BF16.
 //
-// Mega-MoE page: combine_quantizer "fake-quantizes the router-weighted per-(token, top-k
-// slot) rows ..., then sums them again in the kernel's order (ascending slot, FP32 from
-// zero, one BF16 rounding; a fused shared expert's slot last and unquantized)".  The same
-// page's layout self-check compares a re-sum with the kernel output bit for bit; inside a
-// captured graph the check runs on the device (moe_combine_verify, which reports through
-// a status word instead of asserting).
+// Mega-MoE page: the combine fake-quantiser acts on the router-weighted per-(token,
+// slot) rows and then re-adds them exactly as the fused kernel does -- slots in increasing
+// order, a float32 accumulator starting at zero, a single rounding to BF16, the fused
+// shared expert last and never quantised.  The same page checks once that such a re-sum
+// equals the kernel's output exactly, and inside a captured graph does the comparison on
+// the device (here moe_combine_verify, which reports through a status word instead of an
+// assert).
 //
 // Every float op is an explicit round-to-nearest intrinsic (__fmul_rn / __fadd_rn /
 // __fdiv_rn) so the compiler cannot contract them into FMAs: the result is bit-exact

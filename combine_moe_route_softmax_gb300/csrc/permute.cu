@@ -1,12 +1,12 @@
 // Permute (dispatch into the expert-major layout): stable counting sort of the valid
 // (token, slot) pairs by expert id, then a gather of each row's token activations.
 //
-// MoonEP page: dispatch returns the rows "already grouped per expert row" ([NvS, H]) plus
-// cu_seqlens, and the experts run as a grouped GEMM over those segments.  Permute-scratch
-// page: the scratch is sized from the inputs actually received and holds index metadata
-// only.  DeepEP page: the low-latency dispatch takes BF16 tokens and, for FP8, quantises
-// them internally and sends "tokens, and scales" -- here the 1x128 quantisation is fused
-// into the row gather.
+// MoonEP page: after dispatch the rows are laid out expert by expert ([NvS, H]) with
+// cu_seqlens marking the segments, and the experts run as a grouped GEMM over them.
+// Permute-scratch page: the scratch is sized from the inputs actually received and
+// carries index data only.  DeepEP page: the low-latency dispatch accepts BF16 tokens and
+// can quantise them to FP8 itself, shipping codes plus scales that the receiver
+// dequantises -- here the 1x128 quantisation is fused into the row gather.
 //
 // Four launches, none of which waits on another block:
 //   count   per-block per-segment histograms             (reads T*K*4 B)

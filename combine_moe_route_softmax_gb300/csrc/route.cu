@@ -1,8 +1,8 @@
 // Router: softmax -> top-k -> renormalise, one warp per token.
 //
-// The DeepEP page carries per-token topk_weights / topk_ids into dispatch and the MoonEP
-// page speaks of "[T, K] IDs"; the router itself is not spelled out, so this is the
-// plain softmax -> top-k -> renormalise reading.  Selection happens on the float32 logits
+// The DeepEP page passes per-token topk_weights / topk_ids into dispatch and the MoonEP
+// page works with [T, K] expert ids; neither defines the router function, so this takes
+// the plain softmax -> top-k -> renormalise reading.  Selection happens on the float32 logits
 // (softmax is monotone): descending, ties to the lower expert id, so the ids are exact.
 // The renormalised weights need only the chosen logits: the full softmax denominator
 // cancels, w_k = e^{l_k - l_max} / sum_j e^{l_j - l_max}.

@@ -21,6 +21,8 @@ lm_eval / OLMoE runs need datasets and trained weights, which these stand in for
 * ``prefill``   T=8192 tokens in a power-of-two bucket of 16384 rows (rows past 8192 are
   padding), H=7168, I=2048, E=256, K=8, one shared expert, BF16; logits N(0,1) plus a
   per-expert bias -1.1*ln(rank+1) over a seeded permutation rank (Zipf(1.1) popularity).
+* ``prefill_small`` the prefill shapes with E=32 and T=2048 tokens in a 4096-row bucket
+  (about 4 GB on the device), for hardware-counter profiles.
 * ``prefill_fq`` the prefill workload with the combine's constant-scale FP8
   fake-quant; the scale comes from a calibration batch drawn with seed + 1.
 
@@ -55,6 +57,9 @@ WORKLOADS = {
     "mid": Workload("mid", 512, 512, 2048, 1408, 64, 8, False, "bf16", "skew", 0.1),
     "decode": Workload("decode", 128, 128, 7168, 2048, 256, 8, True, "e4m3", "uniform", 0.0),
     "prefill": Workload("prefill", 16384, 8192, 7168, 2048, 256, 8, True, "bf16", "zipf", 0.0),
+    # prefill shapes with fewer experts and tokens (about 4 GB on the device): the case
+    # full hardware-counter profiles are taken on
+    "prefill_small": Workload("prefill_small", 4096, 2048, 7168, 2048, 32, 8, True, "bf16", "zipf", 0.0),
     "prefill_fq": Workload("prefill_fq", 16384, 8192, 7168, 2048, 256, 8, True, "bf16", "zipf",
                            0.0, fake_quant=True, graph=True),
 }

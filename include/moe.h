@@ -61,8 +61,8 @@ const char* moe_status_string(moe_status_t s);
 
 /* ---------------------------------------------------------------------------- route
  * Router: softmax over E, top-K, renormalise over the K chosen.
- * [DeepEP] carries per-token topk_weights / topk_ids into dispatch and [MoonEP] speaks
- * of "[T, K] IDs"; neither page spells out the router, so this is the plain
+ * [DeepEP] passes per-token topk_weights / topk_ids into dispatch and [MoonEP] works with
+ * [T, K] expert ids; neither page defines the router function, so this takes the plain
  * softmax -> top-k -> renormalise reading.
  *   logits     float32 [T, E], finite.
  *   num_tokens nullable device int32 scalar n: rows t >= n are padding of a receive
@@ -80,8 +80,8 @@ moe_status_t moe_route_topk(const float* logits, int T, int E, int K, const int3
 
 /* -------------------------------------------------------------------------- permute
  * Dispatch into the expert-major layout: a stable counting sort of the valid
- * (token, slot) pairs by expert id ([MoonEP]: rows "already grouped per expert row",
- * [NvS, H] plus cu_seqlens; [DeepEP]: moe_permute_unpermute), then a gather of each
+ * (token, slot) pairs by expert id ([MoonEP]: after dispatch the rows arrive grouped by
+ * expert, [NvS, H] plus cu_seqlens; [DeepEP]: moe_permute_unpermute), then a gather of each
  * row's token.  Flat slot s = t*K + k; segment e holds the slots with topk_idx == e in
  * ascending s.  topk_idx == -1 marks padding ([MegaMoE]: valid = topk_idx >= 0): no row.
  *
@@ -105,8 +105,8 @@ moe_status_t moe_route_topk(const float* logits, int T, int E, int K, const int3
  *   inv_map    out int32 [T, K]: row of each slot, -1 for padding.
  *   shared_map out int32 [T] (required iff with_shared): shared row of each token, or -1.
  *   ws         scratch of at least moe_permute_workspace_bytes(T, K, E, with_shared) bytes,
- *              256-byte aligned; index metadata only ([Scratch]: the scratch "holds only
- *              index metadata"), no state kept between calls.
+ *              256-byte aligned; it holds index metadata only ([Scratch]: the permute
+ *              scratch carries no hidden states), no state kept between calls.
  *   dev_status nullable; MOE_DEV_BAD_EXPERT is ORed in for ids outside [-1, E).
  * Rows of xp at or past N are not written.
  * Errors: MOE_ERR_ARG for bad sizes / null pointers, MOE_ERR_WORKSPACE if ws_bytes is short. */
@@ -131,8 +131,8 @@ moe_status_t moe_quantize_weight_fp8(const uint16_t* w, int mats, int rows, int 
                                      float* scales, void* stream);
 
 /* ---------------------------------------------------------------------- grouped GEMM
- * Grouped GEMM over the cu_seqlens segments ([MoonEP]: the experts are grouped GEMMs,
- * gate, up and down, "over the cu_seqlens segments"; "empty segments ... are skipped").
+ * Grouped GEMM over the cu_seqlens segments ([MoonEP]: the gate, up and down projections
+ * run as grouped matmuls over the segments, and a segment with no rows costs nothing).
  * For each segment s and each row r in [cu[s], cu[s+1]):
  *     acc[r, n] = sum_k a[r, k] * W_s[n, k]      (FP32 accumulation, tensor cores)
  * W_s = w + s*n_dim*k_dim for s < num_w, and w_extra for s == num_w (the shared expert).
@@ -159,9 +159,9 @@ moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_
                               int32_t* dev_status, void* stream);
 
 /* -------------------------------------------------------------------------- combine
- * Fixed-order combine ([MegaMoE]: the router-weighted per-(token, top-k slot) rows are
- * summed "in the kernel's order (ascending slot, FP32 from zero, one BF16 rounding; a
- * fused shared expert's slot last and unquantized)"):
+ * Fixed-order combine ([MegaMoE]: each token's router-weighted slot rows are added in
+ * increasing slot order into a float32 accumulator that starts at zero, rounded to BF16
+ * a single time, with the fused shared expert added as the final, never-quantised slot):
  *     acc = +0.0f
  *     for k = 0..K-1 with inv_map[t,k] >= 0:
  *         r = float(y[inv_map[t,k]]) * topk_w[t,k]          (float32 product)
@@ -183,8 +183,9 @@ moe_status_t moe_combine(const uint16_t* y, const int32_t* inv_map, const float*
                          int H, const uint16_t* shared_y, const int32_t* shared_map,
                          const float* fq_scale, uint16_t* out, void* stream);
 
-/* Layout self-check ([MegaMoE]: "each buffer checks that its rows reproduce the kernel
- * output bit for bit"; inside a graph the check runs on the device).  Recomputes the
+/* Layout self-check ([MegaMoE]: on the first routed batch the re-summed rows must equal
+ * the kernel's output exactly, and a captured graph performs that comparison on the
+ * device).  Recomputes the
  * combine from the same arguments and compares it bit for bit with `expected`
  * (BF16 [T, H]); any difference ORs MOE_DEV_VERIFY_MISMATCH into dev_status (required).
  * Never asserts or traps. */
@@ -193,8 +194,8 @@ moe_status_t moe_combine_verify(const uint16_t* y, const int32_t* inv_map, const
                                 const float* fq_scale, const uint16_t* expected, int32_t* dev_status,
                                 void* stream);
 
-/* Calibration ([MegaMoE]: algorithm "max"; "the calibrated amax equaled the max of what
- * each quantizer saw"): amax = max(amax, max |float(y[inv_map[t,k]]) * topk_w[t,k]|) over
+/* Calibration ([MegaMoE]: max calibration, whose amax is the largest magnitude the
+ * combine quantiser observes): amax = max(amax, max |float(y[inv_map[t,k]]) * topk_w[t,k]|) over
  * every valid slot.  amax is a device float32 the caller zeroes first; repeated calls
  * accumulate (max).  Exact (max is order-independent). */
 moe_status_t moe_combine_amax(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,

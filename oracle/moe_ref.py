@@ -7,7 +7,7 @@ steps, with no blocking or fusion beyond what the definition states.
 Notation follows the pages: T tokens, H hidden size, I expert intermediate size,
 E routed experts, K = experts per token (top-k), topk_idx / topk_weights [T, K],
 cu_seqlens over expert segments, and the expert-major row layout [NvS, H] of the
-MoonEP page ("dispatch returns tokens already grouped per expert row").
+MoonEP page (after dispatch the rows arrive grouped by expert).
 """
 import numpy as np
 
@@ -22,10 +22,10 @@ STATUS_VERIFY_MISMATCH = 2
 def route_topk(logits, K, num_tokens=None):
     """Router: softmax over the E experts, top-K, renormalise over the chosen K.
 
-    The DeepEP page carries per-token ``topk_weights`` / ``topk_ids`` into dispatch
-    and the MoonEP page speaks of "[T, K] IDs", but neither spells out the router; this
-    is the plain softmax -> top-k -> renormalise reading.  Softmax is computed in fp64;
-    the top K are chosen on the float32 logits (softmax is monotone, so this is the
+    The DeepEP page passes per-token ``topk_weights`` / ``topk_ids`` into dispatch and
+    the MoonEP page works with [T, K] expert ids, but neither defines the router
+    function; this takes the plain softmax -> top-k -> renormalise reading.  Softmax is
+    computed in fp64; the top K are chosen on the float32 logits (softmax is monotone, so this is the
     same set) in descending order, ties going to the lower expert id; the chosen
     probabilities are divided by their sum and rounded once to float32.
 
@@ -54,16 +54,16 @@ def route_topk(logits, K, num_tokens=None):
 def permute(topk_idx, E, with_shared=False):
     """Counting sort of the valid (token, slot) pairs into the expert-major layout.
 
-    MoonEP page: dispatch returns the rows "already grouped per expert row" as
-    [NvS, H] plus cu_seqlens, and expert compute is a grouped GEMM over the cu_seqlens
-    segments.  Flat slot s = t*K + k.  Segment e holds, in ascending s, every slot with
-    topk_idx == e (a stable sort by expert id).  Slots with topk_idx == -1 are padding
+    MoonEP page: after dispatch the rows are laid out expert by expert as [NvS, H]
+    with cu_seqlens marking the segments, and the experts run as a grouped GEMM over
+    those segments.  Flat slot s = t*K + k.  Segment e holds, in ascending s, every
+    slot with topk_idx == e (a stable sort by expert id).  Slots with topk_idx == -1 are padding
     and get no row (the Mega-MoE page's ``valid = topk_idx >= 0`` mask).  An id outside
     [-1, E) is a data error: status bit 0 is set and the slot is treated as padding.
 
     with_shared appends one more segment (index E) for the shared expert: every token
     with at least one valid slot, in ascending t, its source index being T*K + t.
-    (The shared expert is "fused as the last combine slot" on the Mega-MoE page; here
+    (On the Mega-MoE page a fused shared expert occupies the combine's final slot; here
     it runs as one extra dense segment of the same grouped GEMM, like the extra
     [E, E+B) segments of the MoonEP layout.)
 
@@ -126,8 +126,9 @@ def _block_scale(amax):
 def act_quant_1x128(x):
     """Per-row, per-128-column FP8 quantisation of activations.
 
-    The DeepEP page's low-latency dispatch quantises BF16 tokens to FP8 "and scales"
-    and dequantises at the receiver; its DeepGEMM test sizes tiles by block_n x block_k.
+    The DeepEP page's low-latency dispatch can quantise BF16 tokens to FP8 itself,
+    sending codes plus scales that the receiver dequantises; its DeepGEMM test sizes
+    tiles by block_n x block_k.
     The scale format is not stated; this takes an FP32 scale per 1x128 block,
     s = amax / 448, and codes q = e4m3(x / s) (round to nearest even, saturating), with
     the divisions in float32.  Dequantisation is q * s.
@@ -144,7 +145,7 @@ def act_quant_1x128(x):
 
 def weight_quant_128x128(w):
     """FP8 quantisation of a weight matrix [N, K] with one FP32 scale per 128x128 block
-    (the "block_n x block_k" weight tiles of the DeepEP page), same rule as above.
+    (the block_n x block_k weight tiles of the DeepEP page's DeepGEMM test), same rule as above.
     Returns (codes uint8 [N, K], scales float32 [N/128, K/128])."""
     w = np.asarray(w, dtype=F32)
     N, K = w.shape
@@ -226,7 +227,7 @@ def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale
 
 
 def combine_amax(y_bits, inv_map, topk_w):
-    """Calibration ("algorithm: max" on the Mega-MoE page): the largest |r| over every
+    """Calibration (max calibration on the Mega-MoE page): the largest |r| over every
     valid router-weighted row element r = float32(y * w).  0 if there is no valid slot."""
     inv_map = np.asarray(inv_map)
     best = F32(0.0)
@@ -257,8 +258,8 @@ def _f64_weights(w_bits_or_f):
 
 def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
                     fq_scale=None, fp8=False):
-    """Dense per-token reference MoE in fp64 (the MoonEP page checks its path "against a
-    dense per-token reference MoE"): for each token, for the valid slots in ascending
+    """Dense per-token reference MoE in fp64 (the MoonEP page validates its path by
+    comparing with a straightforward per-token MoE): for each token, for the valid slots in ascending
     order, r = w_k * expert_{idx_k}(x_t) (optionally fake-quantised as in the combine);
     the sum of the r, plus the shared expert's output when the token has a valid slot.
     No final rounding: the result is the float64 value the BF16 output approximates.

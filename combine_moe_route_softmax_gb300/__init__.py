@@ -48,6 +48,8 @@ _SIGS = {
     "moe_route_topk": ([_P, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_permute_workspace_bytes": ([_I, _I, _I, _I], _Z),
     "moe_permute": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P], _I),
+    "moe_permute_noalloc_max_scratch_bytes": ([], _Z),
+    "moe_permute_noalloc": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_quantize_act_fp8": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_quantize_weight_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),

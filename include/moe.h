@@ -116,6 +116,27 @@ moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_
                          int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map, int32_t* shared_map,
                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* moe_permute for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is an addition of this library.)  Some callers may not call cudaMalloc:
+ * plugins inside an inference engine that owns every device allocation, code running while
+ * its stream is captured into a CUDA graph, serving paths with a fixed memory budget.  This
+ * variant takes no workspace: its index scratch is a static device array of
+ * moe_permute_noalloc_max_scratch_bytes() bytes (1 MiB) that every GPU loading the library
+ * holds until the process exits.  Arguments and outputs are those of moe_permute.
+ * - Shapes whose scratch (moe_permute_workspace_bytes) exceeds that maximum are rejected
+ *   with MOE_ERR_WORKSPACE before anything is launched (e.g. E = 256 with a shared
+ *   expert fits T up to about 65000 tokens; E = 1024 about 16000).
+ * - The first call on each device looks up the array's device address (cudaGetSymbolAddress
+ *   with that device current) and caches it; make that first call before any stream
+ *   capture begins.  MOE_ERR_CUDA if the lookup fails.
+ * - All calls on a device share the array.  Nothing in it needs to start at zero, but calls
+ *   whose kernels overlap on the GPU (unordered streams) race on it; order them. */
+size_t moe_permute_noalloc_max_scratch_bytes(void);
+moe_status_t moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                 const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp, float* xp_scales,
+                                 int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
+                                 int32_t* shared_map, int32_t* dev_status, void* stream);
+
 /* ---------------------------------------------------------------------- FP8 quantise
  * Activation quantisation per 1x128 block ([DeepEP]: FP8 dispatch of "tokens, and
  * scales" dequantised at the receiver):  x BF16 [rows, cols] -> q E4M3 [rows, cols],

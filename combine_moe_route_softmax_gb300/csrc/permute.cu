@@ -9,12 +9,15 @@
 // dequantises -- here the 1x128 quantisation is fused into the row gather.
 //
 // Four launches, none of which waits on another block:
-//   count   per-block per-segment histograms             (reads T*K*4 B)
-//   scan    one block: per-segment exclusive prefix over blocks + cu_seqlens
+//   count   per-block per-segment histograms -> counts[seg][block]   (reads T*K*4 B)
+//   scan    one block per segment: exclusive prefix over that segment's blocks; the
+//           last block to finish (an atomic ticket, no waiting) scans the segment totals
+//           into cu_seqlens
 //   scatter per-block: per-warp histograms, a warp-level scan, then an ordered walk with
 //           __match_any_sync ranks -> src_row / inv_map / shared_map (stable by slot)
-//   gather  Xp[p] = x[token(p)] with 16-byte vector loads/stores, one warp per row
-//           (BF16 copy, or E4M3 codes + 1x128 scales).  HBM-bound:
+//   gather  source-ordered: one warp per token reads its row once (16-byte loads) and
+//           writes it to every row that holds it (the token's slots and its shared row),
+//           as BF16 or as E4M3 codes + 1x128 scales.  HBM-bound:
 //           T_valid*H*2 read + N*H*(2 | 1 + 4/128) written.
 #include "common.cuh"
 
@@ -30,6 +33,7 @@ __device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E;
 __global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32_t* __restrict__ idx, int T,
                                                                      int K, int E, int with_shared,
                                                                      int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ ticket,
                                                                      int32_t* dev_status) {
   extern __shared__ int hist[];
   const int nseg = E + with_shared;
@@ -53,59 +57,80 @@ __global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32
     }
   }
   if (bad && dev_status) atomicOr(dev_status, MOE_DEV_BAD_EXPERT);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < nseg; i += blockDim.x) counts[(size_t)blockIdx.x * nseg + i] = hist[i];
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) counts[(size_t)i * gridDim.x + blockIdx.x] = hist[i];
 }
 
-// One block of 1024 threads.  counts[b][e] -> global row offset of block b's rows of
-// segment e; cu_seqlens = exclusive prefix of the per-segment totals.
-__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ counts, int nblk, int nseg,
-                                                            int32_t* __restrict__ cu_seqlens) {
-  __shared__ int tot[2 * 1024];
-  __shared__ int warp_sums[32];
-  for (int e = threadIdx.x; e < 2 * 1024; e += blockDim.x) tot[e] = 0;
-  __syncthreads();
-  for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      const int c = counts[(size_t)b * nseg + e];
-      counts[(size_t)b * nseg + e] = run;
-      run += c;
-    }
-    tot[e] = run;
-  }
-  __syncthreads();
-  // exclusive scan of tot[0 .. 2048): thread i owns elements 2i, 2i+1
-  const int i = threadIdx.x;
-  const int a0 = tot[2 * i], a1 = tot[2 * i + 1];
-  int incl = a0 + a1;
-  const int lane = i & 31, warp = i >> 5;
+// Exclusive scan of v over the block's threads; returns this thread's exclusive prefix
+// and (in *total) the block's sum.  blockDim.x == 256.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
   }
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int ws = warp_sums[lane];
+    int ws = lane < 8 ? warp_sums[lane] : 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, ws, off);
-      if (lane >= off) ws += v;
+    for (int off = 1; off < 8; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws += u;
     }
-    warp_sums[lane] = ws;  // inclusive
+    if (lane < 8) warp_sums[lane] = ws;  // inclusive over warps
   }
   __syncthreads();
-  const int excl = incl - (a0 + a1) + (warp > 0 ? warp_sums[warp - 1] : 0);
+  const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[7];
   __syncthreads();
-  tot[2 * i] = excl;
-  tot[2 * i + 1] = excl + a0;
+  return excl;
+}
+
+// One 256-thread block per segment e: counts[e][b] -> exclusive prefix over the blocks b
+// (the row offset of block b's rows within segment e); seg_total[e] = segment size.  The
+// last block to take a ticket scans the totals into cu_seqlens (cu[0] = 0) and resets the
+// ticket.  No block ever waits for another.
+__global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__ counts, int nblk, int nseg,
+                                                           int32_t* __restrict__ seg_total,
+                                                           int32_t* __restrict__ ticket,
+                                                           int32_t* __restrict__ cu_seqlens) {
+  __shared__ int warp_sums[8];
+  __shared__ int last;
+  const int e = blockIdx.x;
+  int32_t* row = counts + (size_t)e * nblk;
+  int running = 0;
+  for (int base = 0; base < nblk; base += 256) {
+    const int b = base + threadIdx.x;
+    const int v = b < nblk ? row[b] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_sums, &tot);
+    if (b < nblk) row[b] = running + ex;
+    running += tot;
+  }
+  if (threadIdx.x == 0) {
+    seg_total[e] = running;
+    __threadfence();
+    last = atomicAdd(ticket, 1) == nseg - 1;
+  }
   __syncthreads();
-  for (int e = threadIdx.x; e <= nseg; e += blockDim.x) cu_seqlens[e] = tot[e];
-  for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
-    const int base = tot[e];
-    for (int b = 0; b < nblk; ++b) counts[(size_t)b * nseg + e] += base;
+  if (!last) return;
+  __threadfence();
+  running = 0;
+  for (int base = 0; base < nseg; base += 256) {
+    const int i = base + threadIdx.x;
+    const int v = i < nseg ? __ldcg(seg_total + i) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_sums, &tot);
+    if (i < nseg) cu_seqlens[i] = running + ex;
+    running += tot;
+  }
+  if (threadIdx.x == 0) {
+    cu_seqlens[nseg] = running;
+    *ticket = 0;
   }
 }
 
@@ -138,7 +163,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
   __syncthreads();
   // 2. each warp's starting row per segment = block offset + earlier warps' counts
   for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
-    int run = offsets[(size_t)blockIdx.x * nseg + e];
+    int run = cu_seqlens[e] + offsets[(size_t)e * gridDim.x + blockIdx.x];
     for (int w = 0; w < kPermWarps; ++w) {
       const int c = whist[w * nseg + e];
       whist[w * nseg + e] = run;
@@ -192,93 +217,152 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     src_row[p] = -1;
 }
 
-__device__ __forceinline__ int row_token(int src, int TK, int K) { return src < TK ? src / K : src - TK; }
+// Destination rows of token t: its valid slots' rows (inv_map) and its shared row.  Lane
+// k < K holds the row of slot k, lane K the shared row (or -1).
+__device__ __forceinline__ int token_dest(const int32_t* __restrict__ inv_map, const int32_t* __restrict__ shared_map,
+                                          int t, int K, int lane) {
+  if (lane < K) return inv_map[(size_t)t * K + lane];
+  if (lane == K && shared_map) return shared_map[t];
+  return -1;
+}
 
+// Source-ordered gather: one warp per token, the row read once in chunks of 4 16-byte
+// vectors per lane and written to each destination row.
 __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t* __restrict__ x, int T, int K,
-                                                                  int H, const int32_t* __restrict__ src_row,
-                                                                  const int32_t* __restrict__ cu_seqlens,
-                                                                  int nseg, uint16_t* __restrict__ xp) {
+                                                                  int H, const int32_t* __restrict__ inv_map,
+                                                                  const int32_t* __restrict__ shared_map,
+                                                                  uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int total = cu_seqlens[nseg];
   const int nvec = H / 8;
-  for (int p = gw; p < total; p += nw) {
-    const int t = row_token(src_row[p], T * K, K);
+  const int ndst = K + 1;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+    const int my_dst = token_dest(inv_map, shared_map, t, K, lane);
+    const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
+    if (!live) continue;                      // padding token: nothing to copy
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    uint4* o = reinterpret_cast<uint4*>(xp + (size_t)p * H);
-    int v = lane;
-    for (; v + 96 < nvec; v += 128) {
-      const uint4 a = __ldg(in + v), b = __ldg(in + v + 32), c = __ldg(in + v + 64), d = __ldg(in + v + 96);
-      o[v] = a;
-      o[v + 32] = b;
-      o[v + 64] = c;
-      o[v + 96] = d;
-    }
-    for (; v < nvec; v += 32) o[v] = __ldg(in + v);
-  }
-}
-
-// One 1x128 block per half-warp: lane l of a half-warp converts elements [8l, 8l+8).
-__device__ __forceinline__ void quant_row_1x128(const uint16_t* __restrict__ in, uint8_t* __restrict__ q,
-                                                float* __restrict__ scales, int H, int lane) {
-  const int nvec = H / 8;
-  for (int v0 = 0; v0 < nvec; v0 += 32) {
-    const int v = v0 + lane;
-    const bool live = v < nvec;
-    float f[8];
-    float amax = 0.0f;
-    if (live) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(in) + v);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    for (int v0 = 0; v0 < nvec; v0 += 128) {
+      uint4 r[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + lane + 32 * j;
+        if (v < nvec) r[j] = __ldg(in + v);
       }
+      unsigned m = live;
+      while (m) {
+        const int d = __ffs(m) - 1;
+        m &= m - 1;
+        const int row = __shfl_sync(0xffffffffu, my_dst, d);
+        uint4* o = reinterpret_cast<uint4*>(xp + (size_t)row * H);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (live) {
-      const float s = block_scale(amax);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
-      reinterpret_cast<uint2*>(q)[v] = make_uint2(lo, hi);
-      if ((lane & 15) == 0) scales[v / 16] = s;
+        for (int j = 0; j < 4; ++j) {
+          const int v = v0 + lane + 32 * j;
+          if (v < nvec) o[v] = r[j];
+        }
+      }
     }
   }
 }
 
+// 1x128 quantisation of 8 elements per lane (a half-warp covers one 128-block): returns
+// the 8 codes packed in a uint2 and the block's scale.  Every lane of the warp calls it.
+__device__ __forceinline__ uint2 quant8(const uint4 u, bool live, float* scale) {
+  float f[8];
+  float amax = 0.0f;
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = block_scale(amax);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
+  *scale = s;
+  return make_uint2(lo, hi);
+}
+
+// Source-ordered gather with the 1x128 E4M3 quantisation: each token is quantised once and
+// its codes and scales written to every destination row.
 __global__ void __launch_bounds__(256) permute_gather_e4m3_kernel(const uint16_t* __restrict__ x, int T, int K,
-                                                                  int H, const int32_t* __restrict__ src_row,
-                                                                  const int32_t* __restrict__ cu_seqlens,
-                                                                  int nseg, uint8_t* __restrict__ xp,
+                                                                  int H, const int32_t* __restrict__ inv_map,
+                                                                  const int32_t* __restrict__ shared_map,
+                                                                  uint8_t* __restrict__ xp,
                                                                   float* __restrict__ xp_scales) {
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int total = cu_seqlens[nseg];
-  for (int p = gw; p < total; p += nw) {
-    const int t = row_token(src_row[p], T * K, K);
-    quant_row_1x128(x + (size_t)t * H, xp + (size_t)p * H, xp_scales + (size_t)p * (H / 128), H, lane);
+  const int nvec = H / 8;
+  const int nblk = H / 128;
+  const int ndst = K + 1;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+    const int my_dst = token_dest(inv_map, shared_map, t, K, lane);
+    const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
+    if (!live) continue;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool ok = v < nvec;
+      const uint4 u = ok ? __ldg(in + v) : make_uint4(0, 0, 0, 0);
+      float s;
+      const uint2 q = quant8(u, ok, &s);
+      unsigned m = live;
+      while (m) {
+        const int d = __ffs(m) - 1;
+        m &= m - 1;
+        const int row = __shfl_sync(0xffffffffu, my_dst, d);
+        if (ok) {
+          reinterpret_cast<uint2*>(xp + (size_t)row * H)[v] = q;
+          if ((lane & 15) == 0) xp_scales[(size_t)row * nblk + v / 16] = s;
+        }
+      }
+    }
   }
 }
 
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int rows, int cols,
                                                         uint8_t* __restrict__ q, float* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int r = gw; r < rows; r += nw)
-    quant_row_1x128(x + (size_t)r * cols, q + (size_t)r * cols, scales + (size_t)r * (cols / 128), cols, lane);
+  const int nvec = cols / 8;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)r * cols);
+    for (int v0 = 0; v0 < nvec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool ok = v < nvec;
+      float s;
+      const uint2 c = quant8(ok ? __ldg(in + v) : make_uint4(0, 0, 0, 0), ok, &s);
+      if (ok) {
+        reinterpret_cast<uint2*>(q + (size_t)r * cols)[v] = c;
+        if ((lane & 15) == 0) scales[(size_t)r * (cols / 128) + v / 16] = s;
+      }
+    }
+  }
 }
 
 inline int perm_blocks(int T) { return (T + kChunkTok - 1) / kChunkTok; }
+
+// Index scratch: counts [nseg][nblk] | segment totals [nseg] | ticket (256-byte regions).
+struct ScratchLayout {
+  size_t counts, seg_total, ticket, total;
+};
+inline ScratchLayout scratch_layout(size_t nblk, size_t nseg) {
+  auto a = [](size_t x) { return (x + 255) / 256 * 256; };
+  ScratchLayout l;
+  l.counts = 0;
+  l.seg_total = a(nblk * nseg * sizeof(int32_t));
+  l.ticket = l.seg_total + a(nseg * sizeof(int32_t));
+  l.total = l.ticket + 256;
+  return l;
+}
 
 }  // namespace moe
 
@@ -286,8 +370,7 @@ extern "C" size_t moe_permute_workspace_bytes(int T, int K, int E, int with_shar
   using namespace moe;
   if (T < 0 || K < 1 || E < 1 || E > kMaxExperts) return 0;
   const size_t nseg = (size_t)E + (with_shared ? 1 : 0);
-  const size_t bytes = (size_t)perm_blocks(T) * nseg * sizeof(int32_t);
-  return ((bytes + 255) / 256) * 256 + 256;
+  return scratch_layout(perm_blocks(T), nseg).total;
 }
 
 extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_shared,
@@ -312,13 +395,17 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
   if ((size_t)T * K + T > 0x7fffffffull) return MOE_ERR_ARG;
   const size_t need = moe_permute_workspace_bytes(T, K, E, with_shared);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
-  int32_t* counts = static_cast<int32_t*>(ws);
   const int nblk = perm_blocks(T);
+  const ScratchLayout lay = scratch_layout(nblk, nseg);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* counts = reinterpret_cast<int32_t*>(base + lay.counts);
+  int32_t* seg_total = reinterpret_cast<int32_t*>(base + lay.seg_total);
+  int32_t* ticket = reinterpret_cast<int32_t*>(base + lay.ticket);
   const int cap = T * K + (with_shared ? T : 0);
   permute_count_kernel<<<nblk, kPermThreads, nseg * sizeof(int), s>>>(topk_idx, T, K, E, with_shared, counts,
-                                                                        dev_status);
+                                                                        ticket, dev_status);
   MOE_CHECK_LAUNCH();
-  permute_scan_kernel<<<1, 1024, 0, s>>>(counts, nblk, nseg, cu_seqlens);
+  permute_scan_kernel<<<nseg, 256, 0, s>>>(counts, nblk, nseg, seg_total, ticket, cu_seqlens);
   MOE_CHECK_LAUNCH();
   const size_t scatter_smem = (size_t)kPermWarps * nseg * sizeof(int);
   static bool attr_set = false;
@@ -329,13 +416,13 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
   permute_scatter_kernel<<<nblk, kPermThreads, scatter_smem, s>>>(topk_idx, T, K, E, with_shared, counts,
                                                                   cu_seqlens, cap, src_row, inv_map, shared_map);
   MOE_CHECK_LAUNCH();
-  const int gblocks = num_sms() * 8;
+  const int gblocks = min((T + 7) / 8, num_sms() * 8);
+  const int32_t* smap = with_shared ? shared_map : nullptr;
   if (out_dtype == MOE_BF16)
-    permute_gather_bf16_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, src_row, cu_seqlens, nseg,
-                                                       static_cast<uint16_t*>(xp));
+    permute_gather_bf16_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint16_t*>(xp));
   else
-    permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, src_row, cu_seqlens, nseg,
-                                                       static_cast<uint8_t*>(xp), xp_scales);
+    permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint8_t*>(xp),
+                                                       xp_scales);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

@@ -272,29 +272,70 @@ def run_ours(args, rank, world, local_rank):
         t = statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
         stage_ms[name] = max_over_ranks(t, world, device)
 
-    # --- timed region 3: end to end through moe_layer_forward with host buffers
+    # --- timed region 3: end to end through moe_layer_forward with host buffers.  A serving
+    # pipeline: the next batch's inputs are copied in (pinned host -> device, copy stream)
+    # and the previous batch's output copied out (device -> pinned host, a second copy
+    # stream) while the current batch computes; input and output buffers are doubled.
     h_logits = st["logits"].cpu().pin_memory()
     h_x = st["x"].cpu().pin_memory()
-    h_out = torch.empty(st["out"].shape, dtype=torch.bfloat16).pin_memory()
-    d_logits, d_x = torch.empty_like(st["logits"]), torch.empty_like(st["x"])
-    for _ in range(2):
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        layer_step(st, x=d_x, logits=d_logits)
-        h_out.copy_(st["out"], non_blocking=True)
+    h_out = [torch.empty(st["out"].shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_logits = [torch.empty_like(st["logits"]) for _ in range(2)]
+    d_x = [torch.empty_like(st["x"]) for _ in range(2)]
+    d_out = [torch.empty_like(st["out"]) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipeline(n):
+        ev = lambda: torch.cuda.Event()
+        in_ready, comp_done, out_done = [ev(), ev()], [None, None], [None, None]
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(comp)
+        h2d.wait_event(start)
+        d2h.wait_event(start)
+        with torch.cuda.stream(h2d):
+            d_logits[0].copy_(h_logits, non_blocking=True)
+            d_x[0].copy_(h_x, non_blocking=True)
+            in_ready[0].record(h2d)
+        for i in range(n):
+            b = i % 2
+            comp.wait_event(in_ready[b])
+            if out_done[b] is not None:
+                comp.wait_event(out_done[b])          # d_out[b] has been copied out
+            layer_step(st, x=d_x[b], logits=d_logits[b], out=d_out[b])
+            comp_done[b] = ev()
+            comp_done[b].record(comp)
+            if i + 1 < n:
+                nb = (i + 1) % 2
+                with torch.cuda.stream(h2d):
+                    if comp_done[nb] is not None:
+                        h2d.wait_event(comp_done[nb])  # step i-1 no longer reads this input set
+                    d_logits[nb].copy_(h_logits, non_blocking=True)
+                    d_x[nb].copy_(h_x, non_blocking=True)
+                    in_ready[nb] = ev()
+                    in_ready[nb].record(h2d)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(comp_done[b])
+                h_out[b].copy_(d_out[b], non_blocking=True)
+                out_done[b] = ev()
+                out_done[b].record(d2h)
+        for b in range(2):
+            if out_done[b] is not None:
+                comp.wait_event(out_done[b])
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(comp)
+        return start, end
+
+    pipeline(3)
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    e0.record()
-    for _ in range(args.steps):
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        layer_step(st, x=d_x, logits=d_logits)
-        h_out.copy_(st["out"], non_blocking=True)
-    e1.record()
+    e0, e1 = pipeline(args.steps)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
     assert st["status"].item() == 0
+    # the pipelined run's last output reached the host intact (same batch, deterministic kernels)
+    assert torch.equal(h_out[(args.steps - 1) % 2], st["out"].cpu())
 
     if rank != 0:
         return
@@ -352,7 +393,8 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
         "e2e": {"value": round(tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
-                "d2h_bytes_per_step": h_out.numel() * 2},
+                "d2h_bytes_per_step": h_out[0].numel() * 2,
+                "pipeline": "inputs of step i+1 copied in and output of step i-1 copied out during step i"},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

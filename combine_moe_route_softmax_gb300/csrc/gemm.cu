@@ -52,6 +52,9 @@ constexpr int TMEM_COLS = 512;
 constexpr int MAX_SEG = kMaxExperts + 1;
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 
+constexpr int STAGE_OUT_PITCH = 80;                // 64 B of BF16 per row + 16 B pad (conflict-free)
+constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
+
 struct SmemLayout {
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_BYTES;
@@ -62,7 +65,8 @@ struct SmemLayout {
   static constexpr int xch = abort_flag + 12;                 // float [2][128], 16-aligned
   static constexpr int cu = xch + 2 * 128 * 4;                // int [MAX_SEG + 1]
   static constexpr int prefix = cu + (MAX_SEG + 1) * 4;       // int [MAX_SEG + 1]
-  static constexpr int end = prefix + (MAX_SEG + 1) * 4;
+  static constexpr int stage_out = (prefix + (MAX_SEG + 1) * 4 + 15) / 16 * 16;  // per epilogue warp: 32 x 80 B
+  static constexpr int end = stage_out + EPI_WARPS * STAGE_OUT_BYTES;
 };
 constexpr size_t SMEM_BYTES = SmemLayout::end + 1024;           // + alignment slack
 
@@ -234,6 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* xch = reinterpret_cast<float*>(smem + SmemLayout::xch);
   int* cu_s = reinterpret_cast<int*>(smem + SmemLayout::cu);
   int* prefix = reinterpret_cast<int*>(smem + SmemLayout::prefix);
+  uint8_t* stage_out = smem + SmemLayout::stage_out;
 
   const int nseg = args.nseg;
   for (int i = tid; i <= nseg; i += THREADS) cu_s[i] = args.cu[i];
@@ -506,17 +511,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (half == 0) args.out_scales[(size_t)row * (out_cols / 128) + w.nt] = s;
           }
         }
-      } else {
-        if (row_ok && cols_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+      } else if (cols_ok) {
+        // BF16 rows through a per-warp shared-memory transpose: each lane holds one row, but
+        // a store instruction should cover whole sectors, so each 32-column chunk is written
+        // to shared memory row by row and read back as 8 rows x 64 contiguous bytes
+        uint8_t* buf_w = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+        const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
+        for (int c = 0; c < 4; ++c) {
+          uint4* my = reinterpret_cast<uint4*>(buf_w + lane * STAGE_OUT_PITCH);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              o[j] = (uint32_t)f32_to_bf16(acc[8 * v + 2 * j]) | ((uint32_t)f32_to_bf16(acc[8 * v + 2 * j + 1]) << 16);
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+              o[j] = (uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j]) |
+                     ((uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j + 1]) << 16);
+            my[v] = make_uint4(o[0], o[1], o[2], o[3]);
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;                 // row within the warp's 32
+            const int ch = lane & 3;                           // 16-byte chunk of the row's 64 B
+            const uint4 val = *reinterpret_cast<const uint4*>(buf_w + r * STAGE_OUT_PITCH + 16 * ch);
+            if (r < rows_here) {
+              uint16_t* dst = static_cast<uint16_t*>(args.out) + (size_t)(w.row0 + 32 * q + r) * out_cols + col0 + 32 * c;
+              reinterpret_cast<uint4*>(dst)[ch] = val;
+            }
+          }
+          __syncwarp();
         }
       }
     }

@@ -192,6 +192,22 @@ def qdq_f32(r, s):
     return (q / s).astype(F32)
 
 
+# ------------------------------------------------------------------- dispatch fake-quant
+def dispatch_qdq_bits(x_bits, s):
+    """Dispatch fake-quant of BF16 token rows (Mega-MoE page: the dispatch quantiser
+    fake-quantises the tokens the experts receive, with a calibrated or constant global
+    scale).  In float32: t = x * s, snapped to E4M3 (nearest even, saturating), divided by
+    s, and rounded back to BF16 -- the experts' input type here.  Returns BF16 bits."""
+    x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16))
+    return f32_to_bf16_bits(qdq_f32(x, s))
+
+
+def tensor_amax(x_bits):
+    """Calibration of the dispatch scale: the largest |x| of a BF16 tensor (float32)."""
+    x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16))
+    return F32(np.abs(x).max()) if x.size else F32(0.0)
+
+
 # --------------------------------------------------------------------------- combine
 def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale=None):
     """Fixed-order combine (Mega-MoE page): per token, the valid slots in ascending
@@ -203,6 +219,9 @@ def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale
     is inv_map[t, k] (-1: padding, skipped).  Shared row of token t: shared_bits[t]
     (dense) or shared_bits[shared_map[t]].  A token with no valid slot is a padding
     token: out = +0 and no shared row is added.
+    topk_w None: the rows are already router-weighted (the MoonEP page applies the route
+    weights inside the expert computation, before the down projection's output is
+    combined, so the combine only sums), and r = float(y).
     Returns out bits [T, H] uint16.
     """
     inv_map = np.asarray(inv_map)
@@ -214,7 +233,10 @@ def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale
         rows = inv_map[:, k]
         ok = rows >= 0
         y = bf16_bits_to_f32(y_bits[np.where(ok, rows, 0)])
-        r = (y * np.asarray(topk_w, dtype=F32)[:, k:k + 1]).astype(F32)
+        if topk_w is None:
+            r = y
+        else:
+            r = (y * np.asarray(topk_w, dtype=F32)[:, k:k + 1]).astype(F32)
         if fq_scale is not None:
             r = qdq_f32(r, fq_scale)
         acc = np.where(ok[:, None], (acc + r).astype(F32), acc)
@@ -237,7 +259,7 @@ def combine_amax(y_bits, inv_map, topk_w):
         if not ok.any():
             continue
         y = bf16_bits_to_f32(y_bits[rows[ok]])
-        r = (y * np.asarray(topk_w, dtype=F32)[ok, k:k + 1]).astype(F32)
+        r = y if topk_w is None else (y * np.asarray(topk_w, dtype=F32)[ok, k:k + 1]).astype(F32)
         best = max(best, F32(np.abs(r).max()))
     return F32(best)
 
@@ -257,7 +279,7 @@ def _f64_weights(w_bits_or_f):
 
 
 def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
-                    fq_scale=None, fp8=False):
+                    fq_scale=None, fp8=False, dispatch_scale=None):
     """Dense per-token reference MoE in fp64 (the MoonEP page validates its path by
     comparing with a straightforward per-token MoE): for each token, for the valid slots in ascending
     order, r = w_k * expert_{idx_k}(x_t) (optionally fake-quantised as in the combine);
@@ -269,6 +291,9 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     indices (default all).  fp8=True runs the experts on FP8-quantised operands as the
     FP8 path defines them: x and h quantised per 1x128 block, weights per 128x128 block,
     all dequantised to fp64 (the tighter reference for the FP8 configuration).
+    dispatch_scale: the routed experts see dispatch_qdq_bits(x, s) instead of x; the
+    shared expert keeps the original x (the Mega-MoE page requires the shared expert to be
+    unfused when the dispatch is quantised, since a fused one would read the same tokens).
     Returns float64 [len(tokens), H].
     """
     x = bf16_bits_to_f32(np.asarray(x_bits)).astype(np.float64)
@@ -302,6 +327,10 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
         return dequant(qh, sh, 1) @ w2e.T
 
     xs = prep_x(x[toks])
+    xs_shared = xs
+    if dispatch_scale is not None:
+        xq = dispatch_qdq_bits(np.asarray(x_bits)[toks], dispatch_scale)
+        xs = prep_x(bf16_bits_to_f32(xq).astype(np.float64))
     # expert outputs for every (token, slot) pair of the subset, one expert at a time
     contrib = np.zeros((len(toks), K, H), dtype=np.float64)
     sub_idx = topk_idx[toks]
@@ -320,7 +349,7 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     if shared is not None:
         any_valid = (sub_idx >= 0).any(axis=1)
         if any_valid.any():
-            ys = run_expert(xs[any_valid], prep_w(shared[0]), prep_w(shared[1]))
+            ys = run_expert(xs_shared[any_valid], prep_w(shared[0]), prep_w(shared[1]))
             out[any_valid] += ys
     return out
 

@@ -98,3 +98,40 @@ def test_calibration_amax_and_scale():
     # the largest weighted row element maps to (about) the E4M3 maximum
     assert abs(float(np.float32(amax) * s) - 448.0) <= 448.0 * 2.0 ** -23
     assert fq_scale_from_amax(0.0) == 1.0
+
+
+def test_dispatch_qdq_pins():
+    from oracle.moe_ref import dispatch_qdq_bits, tensor_amax
+    # exactly representable E4M3 values (times a power-of-two scale) pass through
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    v = e4m3_decode(codes) / np.float32(8.0)
+    bits = f32_to_bf16_bits(v)
+    assert np.array_equal(dispatch_qdq_bits(bits, 8.0), bits)
+    # the rounding step is torch's E4M3 cast of the float32 product (library routine)
+    import torch
+    rng = np.random.default_rng(21)
+    x = f32_to_bf16_bits(rng.standard_normal(50000).astype(np.float32))
+    s = np.float32(448.0) / tensor_amax(x)
+    xf = bf16_bits_to_f32(x)
+    t = (xf * s).astype(np.float32)
+    q = torch.from_numpy(t).to(torch.float8_e4m3fn).float().numpy()
+    want = f32_to_bf16_bits((q / s).astype(np.float32))
+    assert np.array_equal(dispatch_qdq_bits(x, s), want)
+    assert tensor_amax(x) == np.abs(xf).max()
+
+
+def test_preweighted_rows_equal_unit_weights():
+    """Rows already router-weighted (topk_w None) reduce to the weighted combine with all
+    weights 1, since float32(y * 1) = y exactly; with fake-quant too."""
+    rng = np.random.default_rng(31)
+    T, H, E, K = 40, 256, 12, 4
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    idx[rng.random((T, K)) < 0.2] = -1
+    cu, src, inv, smap, _ = permute(idx, E, with_shared=True)
+    y = f32_to_bf16_bits(rng.standard_normal((len(src), H)).astype(np.float32))
+    ones = np.ones((T, K), np.float32)
+    for fq in (None, 96.0):
+        a = combine(y, inv, None, shared_bits=y, shared_map=smap, fq_scale=fq)
+        b = combine(y, inv, ones, shared_bits=y, shared_map=smap, fq_scale=fq)
+        assert np.array_equal(a, b)
+    assert combine_amax(y, inv, None) == combine_amax(y, inv, ones)

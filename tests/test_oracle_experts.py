@@ -109,3 +109,23 @@ def test_fp8_reference_error_is_the_fp8_rounding_error():
     rms = np.sqrt(((ref8 - ref) ** 2).mean() / (ref ** 2).mean())
     assert 0.03 < rms < 0.10
     assert max_rel_err(ref8, ref) < 0.15
+
+
+def test_layer_reference_dispatch_fake_quant_routes_quantised_tokens_only():
+    """Routed experts see the fake-quantised tokens, the shared expert the original ones."""
+    from oracle.moe_ref import dispatch_qdq_bits
+    rng = np.random.default_rng(5)
+    T, H, I, E, K = 7, 6, 4, 5, 2
+    xb = f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    idx, w = route_topk(rng.standard_normal((T, E)).astype(np.float32), K)
+    w13 = f32_to_bf16_bits(rng.standard_normal((E, 2 * I, H)).astype(np.float32))
+    w2 = f32_to_bf16_bits(rng.standard_normal((E, H, I)).astype(np.float32))
+    shared = (f32_to_bf16_bits(rng.standard_normal((2 * I, H)).astype(np.float32)),
+              f32_to_bf16_bits(rng.standard_normal((H, I)).astype(np.float32)))
+    s = np.float32(20.0)
+    ref = layer_reference(xb, idx, w, w13, w2, shared=shared, dispatch_scale=s)
+    f = lambda a: bf16_bits_to_f32(a).astype(np.float64)
+    routed_only = brute_layer(f(dispatch_qdq_bits(xb, s)), idx, w, f(w13), f(w2), None)
+    shared_only = np.stack([brute_expert(f(xb)[t], f(shared[0]), f(shared[1])) for t in range(T)])
+    assert np.allclose(ref, routed_only + shared_only, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(ref, layer_reference(xb, idx, w, w13, w2, shared=shared), rtol=1e-3, atol=0)

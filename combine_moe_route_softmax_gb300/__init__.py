@@ -28,7 +28,8 @@ class MoeError(RuntimeError):
 
 
 class LayerDesc(ctypes.Structure):
-    _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I)]
+    _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
+                ("weight_in_down", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -38,7 +39,7 @@ class LayerWeights(ctypes.Structure):
 
 class LayerViews(ctypes.Structure):
     _fields_ = [("xp", _P), ("xp_scales", _P), ("hs", _P), ("hs_scales", _P), ("y", _P), ("cu_seqlens", _P),
-                ("src_row", _P), ("inv_map", _P), ("shared_map", _P), ("cap", _I)]
+                ("src_row", _P), ("inv_map", _P), ("shared_map", _P), ("row_weights", _P), ("cap", _I)]
 
 
 # C signatures (restype int = moe_status_t unless noted)
@@ -50,9 +51,12 @@ _SIGS = {
     "moe_permute": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P], _I),
     "moe_permute_noalloc_max_scratch_bytes": ([], _Z),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_permute_ex": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _P, _P, _P], _I),
+    "moe_amax_bf16": ([_P, _Z, _P, _P], _I),
     "moe_quantize_act_fp8": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_quantize_weight_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_gemm_ex": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_combine_verify": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_combine_amax": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -60,7 +64,7 @@ _SIGS = {
     "moe_layer_workspace_bytes": ([ctypes.POINTER(LayerDesc)], _Z),
     "moe_layer_views": ([ctypes.POINTER(LayerDesc), _P, ctypes.POINTER(LayerViews)], _I),
     "moe_layer_forward": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeights), _P, _P, _P, _P, _P, _P, _P,
-                           _P, _Z, _P, _P], _I),
+                           _P, _P, _Z, _P, _P], _I),
 }
 
 _lib = None
@@ -128,8 +132,10 @@ def moe_permute_workspace_bytes(T, K, E, with_shared):
     return lib().moe_permute_workspace_bytes(T, K, E, int(with_shared))
 
 
-def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, dev_status=None, stream=None):
-    """Returns dict(xp, xp_scales, cu_seqlens, src_row, inv_map, shared_map)."""
+def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, dev_status=None, stream=None,
+                dispatch_scale=None, topk_w=None):
+    """Returns dict(xp, xp_scales, cu_seqlens, src_row, inv_map, shared_map, row_weights).
+    dispatch_scale / topk_w select moe_permute_ex (dispatch fake-quant / row weights)."""
     _dev(topk_idx)
     _dev(x)
     T, K = topk_idx.shape
@@ -147,10 +153,20 @@ def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, 
     nbytes = moe_permute_workspace_bytes(T, K, E, with_shared)
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    _check("moe_permute", lib().moe_permute(
-        _ptr(topk_idx), T, K, E, int(with_shared), _ptr(x), H, out_dtype, _ptr(xp), _ptr(xps), _ptr(cu), _ptr(src),
-        _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
-    return dict(xp=xp, xp_scales=xps, cu_seqlens=cu, src_row=src, inv_map=inv, shared_map=smap)
+    roww = None
+    if dispatch_scale is None and topk_w is None:
+        _check("moe_permute", lib().moe_permute(
+            _ptr(topk_idx), T, K, E, int(with_shared), _ptr(x), H, out_dtype, _ptr(xp), _ptr(xps), _ptr(cu),
+            _ptr(src), _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+            _stream(stream)))
+    else:
+        if topk_w is not None:
+            roww = torch.empty(cap, dtype=torch.float32, device=dev)
+        _check("moe_permute_ex", lib().moe_permute_ex(
+            _ptr(topk_idx), T, K, E, int(with_shared), _ptr(x), H, out_dtype, _ptr(xp), _ptr(xps), _ptr(cu),
+            _ptr(src), _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+            _ptr(dispatch_scale), _ptr(topk_w), _ptr(roww), _stream(stream)))
+    return dict(xp=xp, xp_scales=xps, cu_seqlens=cu, src_row=src, inv_map=inv, shared_map=smap, row_weights=roww)
 
 
 def moe_quantize_act_fp8(x, stream=None):
@@ -176,7 +192,7 @@ def moe_quantize_weight_fp8(w, stream=None):
 
 def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=None, w_extra=None,
                      w_extra_scales=None, epilogue=MOE_EPI_NONE, out=None, out_scales=None, dev_status=None,
-                     stream=None):
+                     stream=None, row_scale=None):
     """a [rows_cap, k] (bf16 or uint8 E4M3 codes); w [num_w, n, k]; returns (out, out_scales)."""
     _dev(a)
     fp8 = a.dtype == torch.uint8
@@ -190,10 +206,16 @@ def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=
         out = torch.empty(rows_cap, out_cols, dtype=odt, device=a.device)
     if fp8 and epilogue == MOE_EPI_SWIGLU and out_scales is None:
         out_scales = torch.empty(rows_cap, out_cols // 128, dtype=torch.float32, device=a.device)
-    _check("moe_grouped_gemm", lib().moe_grouped_gemm(
-        _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
-        num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),
-        _ptr(out_scales), _ptr(dev_status), _stream(stream)))
+    if row_scale is None:
+        _check("moe_grouped_gemm", lib().moe_grouped_gemm(
+            _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
+            num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),
+            _ptr(out_scales), _ptr(dev_status), _stream(stream)))
+    else:
+        _check("moe_grouped_gemm_ex", lib().moe_grouped_gemm_ex(
+            _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
+            num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),
+            _ptr(out_scales), _ptr(dev_status), _ptr(row_scale), _stream(stream)))
     return out, out_scales
 
 
@@ -224,6 +246,12 @@ def moe_combine_amax(y, inv_map, topk_w, amax, stream=None):
     return amax
 
 
+def moe_amax_bf16(x, amax, stream=None):
+    _dev(x)
+    _check("moe_amax_bf16", lib().moe_amax_bf16(_ptr(x), x.numel(), _ptr(amax), _stream(stream)))
+    return amax
+
+
 def moe_fq_scale_from_amax(amax, scale=None, stream=None):
     if scale is None:
         scale = torch.empty(1, dtype=torch.float32, device=amax.device)
@@ -237,8 +265,9 @@ class MoeLayer:
     [H, I]) in BF16, or E4M3 codes with their 128x128 scales for dtype MOE_E4M3."""
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
-                 w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda"):
-        self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None))
+                 w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
+                 weight_in_down=False):
+        self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))
@@ -261,9 +290,9 @@ class MoeLayer:
         return self.ws[off:off + n * torch.empty(0, dtype=dtype).element_size()].view(dtype).view(*shape)
 
     def forward(self, x, out, topk_idx, topk_w, logits=None, num_tokens=None, fq_scale=None, dev_status=None,
-                stream=None):
+                stream=None, dispatch_scale=None):
         _check("moe_layer_forward", lib().moe_layer_forward(
             ctypes.byref(self.desc), ctypes.byref(self.weights), _ptr(logits), _ptr(num_tokens), _ptr(topk_idx),
-            _ptr(topk_w), _ptr(x), _ptr(fq_scale), _ptr(out), _ptr(self.ws), self.ws.numel(), _ptr(dev_status),
-            _stream(stream)))
+            _ptr(topk_w), _ptr(x), _ptr(fq_scale), _ptr(dispatch_scale), _ptr(out), _ptr(self.ws), self.ws.numel(),
+            _ptr(dev_status), _stream(stream)))
         return out

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     float my_w = 0.0f;
     if (lane < K) {
       my_p = inv_map[(size_t)t * K + lane];
-      my_w = topk_w[(size_t)t * K + lane];
+      my_w = topk_w ? topk_w[(size_t)t * K + lane] : 1.0f;   // NULL: rows already weighted
     }
     const unsigned valid = __ballot_sync(0xffffffffu, lane < K && my_p >= 0);
     int srow = -1;
@@ -139,7 +139,7 @@ moe_status_t launch_combine(const uint16_t* y, const int32_t* inv_map, const flo
 inline moe_status_t check_combine_args(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
                                        int K, int H, const uint16_t* shared_y) {
   if (T < 0 || K < 1 || K > kMaxTopK || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
-  if (T > 0 && (!y || !inv_map || !topk_w)) return MOE_ERR_ARG;
+  if (T > 0 && (!y || !inv_map)) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(shared_y)) & 15) return MOE_ERR_ARG;
   return MOE_OK;
 }

@@ -83,6 +83,7 @@ struct Args {
   void* out;
   float* out_scales;
   int32_t* dev_status;
+  const float* row_scale;   // plain epilogue: out row r is multiplied by row_scale[r] (nullable)
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -515,6 +516,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // BF16 rows through a per-warp shared-memory transpose: each lane holds one row, but
         // a store instruction should cover whole sectors, so each 32-column chunk is written
         // to shared memory row by row and read back as 8 rows x 64 contiguous bytes
+        if (args.row_scale) {
+          // router weight of each permuted row, applied to the float32 accumulator
+          const float rs = row_ok ? args.row_scale[row] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
+        }
         uint8_t* buf_w = stage_out + (warp - 2) * STAGE_OUT_BYTES;
         const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
 #pragma unroll
@@ -597,11 +604,12 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMa
 }  // namespace gg
 }  // namespace moe
 
-extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,
-                                         int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
-                                         const float* w_scales, int num_w, const void* w_extra,
-                                         const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
-                                         void* out, float* out_scales, int32_t* dev_status, void* stream) {
+extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                                            int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
+                                            const float* w_scales, int num_w, const void* w_extra,
+                                            const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
+                                            void* out, float* out_scales, int32_t* dev_status,
+                                            const float* row_scale, void* stream) {
   using namespace moe;
   using namespace moe::gg;
   const bool fp8 = dtype == MOE_E4M3;
@@ -612,6 +620,7 @@ extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, c
   if (num_segments > num_w + (w_extra ? 1 : 0)) return MOE_ERR_ARG;
   if (k_dim <= 0 || k_dim % 128 != 0 || n_dim <= 0 || n_dim % 128 != 0) return MOE_ERR_ARG;
   if (swiglu && (n_dim % 256 != 0)) return MOE_ERR_ARG;
+  if (swiglu && row_scale) return MOE_ERR_ARG;
   if (num_segments == 0 || rows_cap == 0) return MOE_OK;
   if (!a || !cu_seqlens || !out || (num_w > 0 && !w)) return MOE_ERR_ARG;
   if (fp8 && (!a_scales || (num_w > 0 && !w_scales) || (w_extra && !w_extra_scales))) return MOE_ERR_ARG;
@@ -643,6 +652,7 @@ extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, c
   args.out = out;
   args.out_scales = out_scales;
   args.dev_status = dev_status;
+  args.row_scale = row_scale;
   // grid: one CTA per SM, never more than the largest possible number of tiles
   const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
@@ -651,4 +661,13 @@ extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, c
   if (fp8)
     return swiglu ? launch<true, true>(ma, mb, mbx, args, grid, s) : launch<true, false>(ma, mb, mbx, args, grid, s);
   return swiglu ? launch<false, true>(ma, mb, mbx, args, grid, s) : launch<false, false>(ma, mb, mbx, args, grid, s);
+}
+
+extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                                         int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
+                                         const float* w_scales, int num_w, const void* w_extra,
+                                         const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
+                                         void* out, float* out_scales, int32_t* dev_status, void* stream) {
+  return moe_grouped_gemm_ex(a, a_scales, cu_seqlens, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
+                             w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, nullptr, stream);
 }

@@ -14,7 +14,7 @@
 namespace moe {
 
 struct LayerPlan {
-  size_t off_cu, off_src, off_inv, off_smap, off_scratch, off_xp, off_xps, off_hs, off_hss, off_y, total;
+  size_t off_cu, off_src, off_inv, off_smap, off_roww, off_scratch, off_xp, off_xps, off_hs, off_hss, off_y, total;
   size_t scratch_bytes;
   int cap, nseg;
 };
@@ -25,6 +25,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
   if (!d) return false;
   if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E < 1 || d->E > kMaxExperts || d->K < 1 || d->K > d->E ||
       d->K > kMaxTopK || d->H % 128 || d->I % 128 || (d->has_shared != 0 && d->has_shared != 1) ||
+      (d->weight_in_down != 0 && d->weight_in_down != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -40,6 +41,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
   p->off_src = o;     o = align256(o + 4 * cap);
   p->off_inv = o;     o = align256(o + 4 * T * K);
   p->off_smap = o;    o = align256(o + 4 * T);
+  p->off_roww = o;    o = align256(o + 4 * cap);
   p->off_scratch = o; o = align256(o + p->scratch_bytes);
   p->off_xp = o;      o = align256(o + cap * H * esz);
   p->off_xps = o;     o = align256(o + (fp8 ? cap * (H / 128) * 4 : 0));
@@ -66,6 +68,7 @@ extern "C" moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe
   v->src_row = reinterpret_cast<int32_t*>(b + p.off_src);
   v->inv_map = reinterpret_cast<int32_t*>(b + p.off_inv);
   v->shared_map = d->has_shared ? reinterpret_cast<int32_t*>(b + p.off_smap) : nullptr;
+  v->row_weights = reinterpret_cast<float*>(b + p.off_roww);
   v->xp = b + p.off_xp;
   v->xp_scales = fp8 ? reinterpret_cast<float*>(b + p.off_xps) : nullptr;
   v->hs = b + p.off_hs;
@@ -77,8 +80,9 @@ extern "C" moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe
 
 extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_layer_weights_t* w,
                                           const float* logits, const int32_t* num_tokens, int32_t* topk_idx,
-                                          float* topk_w, const uint16_t* x, const float* fq_scale, uint16_t* out,
-                                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+                                          float* topk_w, const uint16_t* x, const float* fq_scale,
+                                          const float* dispatch_scale, uint16_t* out, void* ws, size_t ws_bytes,
+                                          int32_t* dev_status, void* stream) {
   using namespace moe;
   LayerPlan p;
   if (!plan_layer(d, &p) || !w) return MOE_ERR_ARG;
@@ -88,6 +92,7 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   if (!topk_idx || !topk_w || !x || !out || !w->w13 || !w->w2) return MOE_ERR_ARG;
   const bool fp8 = d->dtype == MOE_E4M3;
   if (fp8 && (!w->w13_scales || !w->w2_scales)) return MOE_ERR_ARG;
+  if (fp8 && dispatch_scale) return MOE_ERR_UNSUPPORTED;   // the FP8 path already quantises the dispatch
   if (d->has_shared && (!w->shared_w13 || !w->shared_w2 ||
                         (fp8 && (!w->shared_w13_scales || !w->shared_w2_scales))))
     return MOE_ERR_ARG;
@@ -98,9 +103,11 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
     st = moe_route_topk(logits, d->T, d->E, d->K, num_tokens, topk_idx, topk_w, stream);
     if (st != MOE_OK) return st;
   }
-  st = moe_permute(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, v.cu_seqlens,
-                   v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes,
-                   dev_status, stream);
+  const bool wd = d->weight_in_down != 0;
+  st = moe_permute_ex(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales,
+                      v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch,
+                      p.scratch_bytes, dev_status, dispatch_scale, wd ? topk_w : nullptr,
+                      wd ? v.row_weights : nullptr, stream);
   if (st != MOE_OK) return st;
   const void* sx13 = d->has_shared ? w->shared_w13 : nullptr;
   const void* sx2 = d->has_shared ? w->shared_w2 : nullptr;
@@ -108,10 +115,11 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                         sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
                         v.hs_scales, dev_status, stream);
   if (st != MOE_OK) return st;
-  st = moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, w->w2_scales, d->E, sx2,
-                        d->has_shared ? w->shared_w2_scales : nullptr, d->dtype, MOE_EPI_NONE, v.y, nullptr,
-                        dev_status, stream);
+  st = moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, w->w2_scales, d->E,
+                           sx2, d->has_shared ? w->shared_w2_scales : nullptr, d->dtype, MOE_EPI_NONE, v.y, nullptr,
+                           dev_status, wd ? v.row_weights : nullptr, stream);
   if (st != MOE_OK) return st;
-  return moe_combine(v.y, v.inv_map, topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr, v.shared_map,
-                     fq_scale, out, stream);
+  // with the router weights applied in the down projection the combine only sums
+  return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
+                     v.shared_map, fq_scale, out, stream);
 }

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__
 __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     const int32_t* __restrict__ idx, int T, int K, int E, int with_shared, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ cu_seqlens, int cap, int32_t* __restrict__ src_row, int32_t* __restrict__ inv_map,
-    int32_t* __restrict__ shared_map) {
+    int32_t* __restrict__ shared_map, const float* __restrict__ topk_w, float* __restrict__ row_w) {
   extern __shared__ int whist[];  // [kPermWarps][nseg]
   const int nseg = E + with_shared;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
       rank = __popc(peers & lanemask_lt());
       const int pos = my[e] + rank;
       src_row[pos] = s;
+      if (row_w) row_w[pos] = topk_w[s];
       inv_map[s] = pos;
     } else if (inr) {
       inv_map[s] = -1;
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
       if (any) {
         const int pos = my[E] + __popc(ball & lanemask_lt());
         src_row[pos] = T * K + t;
+        if (row_w) row_w[pos] = 1.0f;
         shared_map[t] = pos;
       } else if (inr) {
         shared_map[t] = -1;
@@ -226,38 +228,60 @@ __device__ __forceinline__ int token_dest(const int32_t* __restrict__ inv_map, c
   return -1;
 }
 
+// Dispatch fake-quant of 8 BF16 values: bf16(e4m3(x * s) / s), float32 steps.
+__device__ __forceinline__ uint4 qdq8(const uint4 u, float s) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    const float ql = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(lo, s))), s);
+    const float qh = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(hi, s))), s);
+    o[i] = (uint32_t)f32_to_bf16(ql) | ((uint32_t)f32_to_bf16(qh) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Source-ordered gather: one warp per token, the row read once in chunks of 4 16-byte
-// vectors per lane and written to each destination row.
+// vectors per lane and written to each destination row.  With a dispatch scale (DQ), the
+// routed destinations get the fake-quantised row and the shared row the original.
+template <bool DQ>
 __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t* __restrict__ x, int T, int K,
                                                                   int H, const int32_t* __restrict__ inv_map,
                                                                   const int32_t* __restrict__ shared_map,
+                                                                  const float* __restrict__ dq_scale,
                                                                   uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / 8;
   const int ndst = K + 1;
+  const float s = DQ ? *dq_scale : 1.0f;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
     const int my_dst = token_dest(inv_map, shared_map, t, K, lane);
     const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
     if (!live) continue;                      // padding token: nothing to copy
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     for (int v0 = 0; v0 < nvec; v0 += 128) {
-      uint4 r[4];
+      uint4 r[4], q[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int v = v0 + lane + 32 * j;
-        if (v < nvec) r[j] = __ldg(in + v);
+        if (v < nvec) {
+          r[j] = __ldg(in + v);
+          if (DQ) q[j] = qdq8(r[j], s);
+        }
       }
       unsigned m = live;
       while (m) {
         const int d = __ffs(m) - 1;
         m &= m - 1;
         const int row = __shfl_sync(0xffffffffu, my_dst, d);
+        const bool routed = d < K;
         uint4* o = reinterpret_cast<uint4*>(xp + (size_t)row * H);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int v = v0 + lane + 32 * j;
-          if (v < nvec) o[v] = r[j];
+          if (v < nvec) o[v] = (DQ && routed) ? q[j] : r[j];
         }
       }
     }
@@ -373,12 +397,12 @@ extern "C" size_t moe_permute_workspace_bytes(int T, int K, int E, int with_shar
   return scratch_layout(perm_blocks(T), nseg).total;
 }
 
-extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_shared,
-                                    const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp,
-                                    float* xp_scales, int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
-                                    int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
-                                    void* stream) {
-  using namespace moe;
+namespace moe {
+static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with_shared, const uint16_t* x,
+                                 int H, moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens,
+                                 int32_t* src_row, int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, const float* dq_scale, const float* topk_w, float* row_w,
+                                 void* stream) {
   if (T < 0 || K < 1 || K > kMaxTopK || E < 1 || E > kMaxExperts || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
   if (with_shared != 0 && with_shared != 1) return MOE_ERR_ARG;
   if (out_dtype != MOE_BF16 && out_dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -391,6 +415,8 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
   }
   if (!topk_idx || !x || !xp || !src_row || !inv_map || (with_shared && !shared_map)) return MOE_ERR_ARG;
   if (out_dtype == MOE_E4M3 && !xp_scales) return MOE_ERR_ARG;
+  if (dq_scale && out_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (row_w && !topk_w) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xp)) & 15) return MOE_ERR_ARG;
   if ((size_t)T * K + T > 0x7fffffffull) return MOE_ERR_ARG;
   const size_t need = moe_permute_workspace_bytes(T, K, E, with_shared);
@@ -414,17 +440,44 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
     attr_set = true;
   }
   permute_scatter_kernel<<<nblk, kPermThreads, scatter_smem, s>>>(topk_idx, T, K, E, with_shared, counts,
-                                                                  cu_seqlens, cap, src_row, inv_map, shared_map);
+                                                                  cu_seqlens, cap, src_row, inv_map, shared_map,
+                                                                  topk_w, row_w);
   MOE_CHECK_LAUNCH();
   const int gblocks = min((T + 7) / 8, num_sms() * 8);
   const int32_t* smap = with_shared ? shared_map : nullptr;
   if (out_dtype == MOE_BF16)
-    permute_gather_bf16_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint16_t*>(xp));
+    if (dq_scale)
+      permute_gather_bf16_kernel<true><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
+                                                               static_cast<uint16_t*>(xp));
+    else
+      permute_gather_bf16_kernel<false><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, nullptr,
+                                                                static_cast<uint16_t*>(xp));
   else
     permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint8_t*>(xp),
                                                        xp_scales);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
+}
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                    const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp,
+                                    float* xp_scales, int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
+                                    int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    void* stream) {
+  return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
+                           inv_map, shared_map, ws, ws_bytes, dev_status, nullptr, nullptr, nullptr, stream);
+}
+
+extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                       const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp,
+                                       float* xp_scales, int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
+                                       int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                       const float* dispatch_scale, const float* topk_w, float* row_weights,
+                                       void* stream) {
+  return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
+                           inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights,
+                           stream);
 }
 
 extern "C" moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,

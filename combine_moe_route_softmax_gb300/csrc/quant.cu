@@ -3,6 +3,8 @@
 // q = e4m3_rn_satfinite(w / s).  A one-time weight-preparation call, outside the layer.
 // One 256-thread block per 128x128 tile: each thread reads 64 elements as 8 16-byte
 // vectors, the block reduces the tile's amax, then every thread writes its codes.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -60,6 +62,39 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
 
 }  // namespace moe
 
+namespace moe {
+// max |x| over a BF16 tensor -> atomicMax on the float bits of *amax (non-negative floats
+// order like their bit patterns as signed ints).
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x, size_t n,
+                                                        float* __restrict__ amax) {
+  float m = 0.0f;
+  const size_t nv = n / 8;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < nv; v += stride) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(x) + v);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+  }
+  for (size_t i = nv * 8 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    m = fmaxf(m, fabsf(bf16_to_f32(x[i])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(reinterpret_cast<int*>(amax), __float_as_int(m));
+}
+}  // namespace moe
+
+extern "C" moe_status_t moe_amax_bf16(const uint16_t* x, size_t n, float* amax, void* stream) {
+  using namespace moe;
+  if (!amax || (n > 0 && !x) || (reinterpret_cast<uintptr_t>(x) & 15)) return MOE_ERR_ARG;
+  if (n == 0) return MOE_OK;
+  const size_t blocks = std::min<size_t>((n / 8 + 255) / 256 + 1, (size_t)num_sms() * 8);
+  amax_bf16_kernel<<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(x, n, amax);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 extern "C" moe_status_t moe_quantize_weight_fp8(const uint16_t* w, int mats, int rows, int cols, uint8_t* q,
                                                 float* scales, void* stream) {
   using namespace moe;
@@ -74,7 +109,7 @@ extern "C" moe_status_t moe_quantize_weight_fp8(const uint16_t* w, int mats, int
   return MOE_OK;
 }
 
-extern "C" int moe_abi_version(void) { return 1; }
+extern "C" int moe_abi_version(void) { return 2; }
 
 extern "C" const char* moe_status_string(moe_status_t s) {
   switch (s) {

@@ -54,7 +54,8 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 #define MOE_DEV_VERIFY_MISMATCH 2   /* moe_combine_verify found an element that differs */
 #define MOE_DEV_PIPELINE_TIMEOUT 4  /* a GEMM pipeline wait gave up; its output is invalid */
 
-/* Version of this ABI (bumped on any signature change). */
+/* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
+ * dispatch fake-quant options). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -137,6 +138,28 @@ moe_status_t moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, i
                                  int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
                                  int32_t* shared_map, int32_t* dev_status, void* stream);
 
+/* moe_permute with two options (ABI 2):
+ *   dispatch_scale nullable device float32 s: dispatch fake-quant ([MegaMoE]: the dispatch
+ *              quantiser fake-quantises the tokens the routed experts receive, with a
+ *              calibrated or constant global scale; the shared expert must not see them,
+ *              so the shared rows keep the original x).  Routed rows become
+ *              bf16(float(e4m3_rn_satfinite(x * s)) / s), float32 steps.  BF16 output only
+ *              (MOE_ERR_UNSUPPORTED for E4M3, whose rows are quantised anyway).
+ *   topk_w / row_weights  nullable; with both given, row_weights float32 [cap] receives each
+ *              row's router weight (topk_w[t, k] of its slot, 1 for a shared row), for a down
+ *              projection that applies the weights itself (moe_grouped_gemm_ex row_scale).
+ * Everything else as moe_permute. */
+moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                            const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp, float* xp_scales,
+                            int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map, int32_t* shared_map,
+                            void* ws, size_t ws_bytes, int32_t* dev_status, const float* dispatch_scale,
+                            const float* topk_w, float* row_weights, void* stream);
+
+/* Calibration of the dispatch scale: amax = max(amax, max |x|) over a BF16 tensor of n
+ * elements (16-byte aligned).  amax is a device float32 the caller zeroes; then
+ * moe_fq_scale_from_amax gives 448 / amax. */
+moe_status_t moe_amax_bf16(const uint16_t* x, size_t n, float* amax, void* stream);
+
 /* ---------------------------------------------------------------------- FP8 quantise
  * Activation quantisation per 1x128 block ([DeepEP]: FP8 dispatch of "tokens, and
  * scales" dequantised at the receiver):  x BF16 [rows, cols] -> q E4M3 [rows, cols],
@@ -179,6 +202,18 @@ moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_
                               moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
                               int32_t* dev_status, void* stream);
 
+/* moe_grouped_gemm with a per-row output scale (ABI 2): row_scale nullable float32
+ * [rows_cap]; with MOE_EPI_NONE the float32 accumulator of out row r is multiplied by
+ * row_scale[r] before the BF16 rounding.  This applies the router weights inside the
+ * down projection ([MoonEP]: route weights applied in the expert computation, so the
+ * combine only sums); rejected (MOE_ERR_ARG) with MOE_EPI_SWIGLU. */
+moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                                 int num_segments, int rows_cap, int k_dim, int n_dim,
+                                 const void* w, const float* w_scales, int num_w,
+                                 const void* w_extra, const float* w_extra_scales,
+                                 moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
+                                 int32_t* dev_status, const float* row_scale, void* stream);
+
 /* -------------------------------------------------------------------------- combine
  * Fixed-order combine ([MegaMoE]: each token's router-weighted slot rows are added in
  * increasing slot order into a float32 accumulator that starts at zero, rounded to BF16
@@ -192,7 +227,8 @@ moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_
  *     out[t] = bf16_rn(acc)                   (a token with no valid slot gets +0)
  *   y          BF16 [rows, H] expert outputs in the permuted layout.
  *   inv_map    int32 [T, K] from moe_permute (-1 = padding slot, never read).
- *   topk_w     float32 [T, K].
+ *   topk_w     float32 [T, K]; NULL when the rows are already router-weighted (then
+ *              r = float(y[...]), the same result as weights of 1).
  *   shared_y   nullable BF16: the shared expert's rows; row of token t is shared_map[t]
  *              when shared_map is given (e.g. y itself with moe_permute's shared_map),
  *              else t.
@@ -234,6 +270,8 @@ typedef struct {
   int H, I, E, K;
   moe_dtype_t dtype;  /* MOE_BF16, or MOE_E4M3 (weights and activations FP8, 128-blocks) */
   int has_shared;     /* 1: one shared expert, added last in the combine, never quantised */
+  int weight_in_down; /* 1: router weights applied in the down projection's epilogue (rows
+                         stored weighted in BF16, the combine only sums); 0: in the combine */
 } moe_layer_desc_t;
 
 typedef struct {
@@ -256,6 +294,7 @@ typedef struct {
   int32_t* src_row;             /* [cap] */
   int32_t* inv_map;             /* [T, K] */
   int32_t* shared_map;          /* [T] or NULL */
+  float* row_weights;           /* [cap] router weight per row (weight_in_down) */
   int cap;                      /* T*K + (has_shared ? T : 0) */
 } moe_layer_views_t;
 
@@ -269,12 +308,15 @@ moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe_layer_view
  *              moe_route_topk) and write topk_idx / topk_w; NULL: topk_idx / topk_w are
  *              inputs (e.g. routed elsewhere, with padding slots set to -1 by the caller).
  *   x          BF16 [T, H];  fq_scale nullable device scalar (combine fake-quant);
+ *   dispatch_scale nullable device scalar (dispatch fake-quant, BF16 layers; see
+ *              moe_permute_ex);
  *   out        BF16 [T, H];  ws / ws_bytes: workspace, 256-byte aligned.
  * Errors: as the step calls; MOE_ERR_WORKSPACE if ws_bytes < moe_layer_workspace_bytes. */
 moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_layer_weights_t* w,
                                const float* logits, const int32_t* num_tokens, int32_t* topk_idx,
-                               float* topk_w, const uint16_t* x, const float* fq_scale, uint16_t* out,
-                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+                               float* topk_w, const uint16_t* x, const float* fq_scale,
+                               const float* dispatch_scale, uint16_t* out, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -144,10 +144,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Multicast variant: the box lands at the same shared-memory offset in every CTA of
+// cta_mask within the cluster and completes the transaction on each one's barrier there.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Arrive (on MMA completion) on the barrier at this offset in every CTA of cta_mask.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 template <bool FP8>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -220,10 +245,11 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, c
 }
 
 // ------------------------------------------------------------------------ kernel
-template <bool FP8, bool SWIGLU>
+template <bool FP8, bool SWIGLU, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmBx, const Args args) {
+                        const __grid_constant__ CUtensorMap tmBx, const __grid_constant__ CUtensorMap tmAh,
+                        const Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -246,7 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (tid == 64) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), PAIR ? 2 : 1);   // PAIR: both CTAs' MMAs must release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -258,6 +284,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
+  // the peer's multicast copies and commits target this CTA's barriers: both CTAs of a
+  // pair initialise theirs before either issues anything
+  if (PAIR) cluster_sync_all();
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
   // per-segment M-tile counts -> exclusive prefix (warp 0)
   if (warp == 0) {
     const int chunk = (nseg + 31) / 32;
@@ -322,7 +352,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
           const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
-          tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
+          if (PAIR) {
+            // the pair works on two n-tiles of the same m-tile: each CTA fetches half of the
+            // A rows once and multicasts it to both
+            tma_load_2d_mc(sa + crank * (A_BYTES / 2), &tmAh, kb * KE, w.row0 + (BM / 2) * crank, bar_full(stage),
+                           0x3);
+          } else {
+            tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
+          }
           tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
           tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
           if (++stage == STAGES) {
@@ -369,7 +406,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t acc = (FP8 ? k : (kb | k)) != 0;
             tc_mma<FP8>(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, acc);
           }
-          tc_commit(bar_empty(stage));
+          if (PAIR)
+            tc_commit_mc(bar_empty(stage), 0x3);   // the stage is free only when both MMAs are done
+          else
+            tc_commit(bar_empty(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -557,6 +597,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  // neither CTA of a pair leaves while the other may still multicast into it
+  if (PAIR) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------------- host side
@@ -572,33 +614,54 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// rows x inner-elements matrix, box = 128 rows x 128 bytes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_t rows) {
+// rows x inner-elements matrix, box = box_rows rows x 128 bytes, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_t rows, uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint64_t esz = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(KB_BYTES / esz), 128};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(KB_BYTES / esz), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, bool SWIGLU>
-moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const Args& args,
-                    int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<FP8, SWIGLU>;
+template <bool FP8, bool SWIGLU, bool PAIR>
+moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
+                        const Args& args, int grid, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr = true;
   }
-  kern<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, bx, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, bx, ah, args) != cudaSuccess) return MOE_ERR_CUDA;
   MOE_CHECK_LAUNCH();
   return MOE_OK;
+}
+
+// CTA pairs (2-CTA clusters sharing A) when the unit count per m-tile is even, so the two
+// CTAs of a pair always hold two n-tiles of one m-tile.
+template <bool FP8, bool SWIGLU>
+moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
+                    const Args& args, int grid, bool pair, cudaStream_t s) {
+  if (pair) return launch_one<FP8, SWIGLU, true>(a, b, bx, ah, args, grid & ~1, s);
+  return launch_one<FP8, SWIGLU, false>(a, b, bx, ah, args, grid, s);
 }
 
 }  // namespace gg
@@ -629,8 +692,9 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
        reinterpret_cast<uintptr_t>(out)) & 15)
     return MOE_ERR_ARG;
   if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
-  CUtensorMap ma, mb, mbx;
+  CUtensorMap ma, mb, mbx, mah;
   if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
+  if (!make_map(&mah, a, fp8, k_dim, rows_cap, BM / 2)) return MOE_ERR_CUDA;
   const void* wb = num_w > 0 ? w : w_extra;
   const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
   if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
@@ -657,10 +721,11 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
   const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
   const int grid = (int)std::min<long long>(num_sms(), max_units);
+  const bool pair = n_tiles % 2 == 0 && grid >= 2;
   cudaStream_t s = as_stream(stream);
   if (fp8)
-    return swiglu ? launch<true, true>(ma, mb, mbx, args, grid, s) : launch<true, false>(ma, mb, mbx, args, grid, s);
-  return swiglu ? launch<false, true>(ma, mb, mbx, args, grid, s) : launch<false, false>(ma, mb, mbx, args, grid, s);
+    return swiglu ? launch<true, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<true, false>(ma, mb, mbx, mah, args, grid, pair, s);
+  return swiglu ? launch<false, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<false, false>(ma, mb, mbx, mah, args, grid, pair, s);
 }
 
 extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,

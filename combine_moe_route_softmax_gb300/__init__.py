@@ -110,11 +110,6 @@ def _dev(t):
     return t
 
 
-def _bits16(t):
-    """BF16 tensor (or its int16/uint16 bit view) -> pointer-compatible tensor."""
-    return _dev(t)
-
-
 # ----------------------------------------------------------------------------- calls
 def moe_route_topk(logits, K, num_tokens=None, topk_idx=None, topk_w=None, stream=None):
     _dev(logits)

@@ -221,7 +221,10 @@ __host__ __device__ constexpr uint32_t instr_desc() {
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and divide: their relative error (a few 1e-6) is far
+// below the BF16 or E4M3 rounding of h that follows; for g < -87 the denominator exceeds
+// 2^126 and the quotient flushes to 0, the limit of g * sigmoid(g).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 struct Unit {
   int seg, row0, row_end, nt;
@@ -452,8 +455,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
       }
       const bool extra = w.seg >= args.num_w;
+      // FP8: a warp whose 32 rows all lie past the segment's end has nothing to promote in
+      // any of the K rounds and only keeps the TMEM hand-off going (decode segments often
+      // hold a few rows).  BF16 has one round per tile and keeps the plain path.
+      const bool warp_live = !FP8 || w.row0 + 32 * q < w.row_end;
       int rounds = FP8 ? kbs_total : 1;
       bool ok = true;
+      // FP8 weight scales of this unit: one row of K-block scales for each 128 weight rows
+      const float* wsc = nullptr;
+      size_t ws0 = 0, ws1 = 0;
+      if (FP8) {
+        wsc = extra ? args.wx_scales : args.w_scales + (size_t)w.seg * (args.n_dim / 128) * kbs_total;
+        if (SWIGLU) {
+          ws0 = (size_t)w.nt * kbs_total;                            // gate rows
+          ws1 = (size_t)(args.n_dim / 256 + w.nt) * kbs_total;       // up rows
+        } else {
+          ws0 = ws1 = (size_t)((w.nt * BN + 128 * half) / 128) * kbs_total;
+        }
+      }
       for (int rd = 0; rd < rounds; ++rd) {
         if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status)) {
           ok = false;
@@ -461,21 +480,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_addr + buf * BN;
-        if (FP8) {
+        if (!warp_live) {
+          // nothing to read
+        } else if (FP8) {
           // promotion of this K block: acc += partial * (s_a[row, kb] * s_w[block, kb])
-          const int kb = rd;
-          const float sa = (row < args.rows_cap) ? args.a_scales[(size_t)row * kbs_total + kb] : 0.0f;
-          const float* wsc = extra ? args.wx_scales : args.w_scales + (size_t)w.seg * (args.n_dim / 128) * kbs_total;
-          float s0, s1;
-          if (SWIGLU) {
-            s0 = wsc[(size_t)w.nt * kbs_total + kb];
-            s1 = wsc[(size_t)(args.n_dim / 256 + w.nt) * kbs_total + kb];
-          } else {
-            const int blk = (w.nt * BN + 128 * half) / 128;
-            s0 = s1 = cols_ok ? wsc[(size_t)blk * kbs_total + kb] : 0.0f;
-          }
-          s0 *= sa;
-          s1 *= sa;
+          const float sa = row_ok ? args.a_scales[(size_t)row * kbs_total + rd] : 0.0f;
+          const float s0 = cols_ok ? wsc[ws0 + rd] * sa : 0.0f;
+          const float s1 = cols_ok ? wsc[ws1 + rd] * sa : 0.0f;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))

@@ -4,6 +4,7 @@ over one batch of the prefill workload (T = 8192 tokens in a 16384-row bucket,
 H = 7168, I = 2048, E = 256, top-8, one shared expert, BF16, Zipf(1.1) router skew).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--layout contiguous|batched [--max-tokens M]]
 
 Prints one JSON line (rank 0).  `value` is layer tokens/s with inputs resident in HBM;
 `e2e` is the same metric through moe_layer_forward with the step's inputs copied from
@@ -134,7 +135,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device):
+def workload_state(w, seed, device, max_tokens=0):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -151,7 +152,7 @@ def workload_state(w, seed, device):
             kw.update(shared_w13=qs13, shared_w2=qs2, shared_w13_scales=cs13, shared_w2_scales=cs2)
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
-    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, **kw)
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, **kw)
     st = dict(layer=layer, logits=logits, x=x,
               idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
               wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
@@ -183,18 +184,38 @@ def staged_step(st, w, events):
     events[0].record()
     assert L.moe_route_topk(p(st["logits"]), d.T, d.E, d.K, p(st["n"]), p(st["idx"]), p(st["wt"]), s) == 0
     events[1].record()
-    scratch_bytes = L.moe_permute_workspace_bytes(d.T, d.K, d.E, d.has_shared)
+    mt = d.max_tokens
+    if mt:
+        scratch_bytes = L.moe_permute_batched_workspace_bytes(d.T, d.K, d.E, d.has_shared)
+    else:
+        scratch_bytes = L.moe_permute_workspace_bytes(d.T, d.K, d.E, d.has_shared)
     scratch = st.setdefault("scratch", torch.empty(scratch_bytes, dtype=torch.uint8, device=st["x"].device))
-    assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp, v.xp_scales,
-                         v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch), scratch_bytes,
-                         p(st["status"]), s) == 0
+    if mt:
+        assert L.moe_permute_batched(p(st["idx"]), d.T, d.K, d.E, d.has_shared, mt, p(st["x"]), d.H, d.dtype, v.xp,
+                                     v.xp_scales, v.masked_m, v.src_row, v.inv_map, v.shared_map, p(scratch),
+                                     scratch_bytes, p(st["status"]), None, None, None, s) == 0
+    else:
+        assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
+                             v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
+                             scratch_bytes, p(st["status"]), s) == 0
     events[2].record()
-    assert L.moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), p(tw[4]), d.E,
-                              p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales, p(st["status"]),
-                              s) == 0
+    if mt:
+        assert L.moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, nseg, mt, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
+                                          d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                          p(st["status"]), None, s) == 0
+    else:
+        assert L.moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
+                                  d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                  p(st["status"]), s) == 0
     events[3].record()
-    assert L.moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]), d.E,
-                              p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]), s) == 0
+    if mt:
+        assert L.moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, nseg, mt, d.I, d.H, p(tw[1]), p(tw[5]),
+                                          d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None,
+                                          p(st["status"]), None, s) == 0
+    else:
+        assert L.moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]),
+                                  d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
+                                  s) == 0
     events[4].record()
     assert L.moe_combine(v.y, v.inv_map, p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None, v.shared_map,
                          None, p(st["out"]), s) == 0
@@ -209,10 +230,13 @@ def algorithmic_work(w, st):
     warm-up, outside the timed regions)."""
     lay = st["layer"]
     d = lay.desc
-    cu = lay.view("cu_seqlens", (d.E + d.has_shared + 1,), torch.int32).cpu().numpy()
-    counts = np.diff(cu)
-    n_routed = int(cu[d.E])
-    n_total = int(cu[-1])
+    nseg = d.E + d.has_shared
+    if d.max_tokens:
+        counts = lay.view("masked_m", (nseg,), torch.int32).cpu().numpy()
+    else:
+        counts = np.diff(lay.view("cu_seqlens", (nseg + 1,), torch.int32).cpu().numpy())
+    n_routed = int(counts[:d.E].sum())
+    n_total = int(counts.sum())
     n_tok = int(counts[d.E]) if d.has_shared else int((st["idx"] >= 0).any(dim=1).sum().item())
     T, K, H, I, E = d.T, d.K, d.H, d.I, d.E
     esz = 1 if w.dtype == "e4m3" else 2
@@ -220,16 +244,12 @@ def algorithmic_work(w, st):
     experts_touched = int((counts[:E] > 0).sum()) + (1 if d.has_shared else 0)
     return {
         "route": {"bytes": T * E * 4 + T * K * 8},
-        "permute": {"bytes": n_tok * H * 2 + n_total * act + T * K * 4 * 2 + v_cap(d) * 4 + T * 4},
+        "permute": {"bytes": n_tok * H * 2 + n_total * act + T * K * 4 * 2 + lay.views.cap * 4 + T * 4},
         "gemm_gate_up": {"flops": 2.0 * n_total * H * 2 * I, "bytes": experts_touched * 2 * I * H * esz},
         "gemm_down": {"flops": 2.0 * n_total * I * H, "bytes": experts_touched * H * I * esz},
         "combine": {"bytes": (n_routed + (n_total - n_routed)) * H * 2 + T * K * 8 + T * H * 2},
         "_rows": {"n_routed": n_routed, "n_total": n_total, "tokens": n_tok, "experts_touched": experts_touched},
     }
-
-
-def v_cap(d):
-    return d.T * d.K + (d.T if d.has_shared else 0)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -238,7 +258,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     dist_init(world, "nccl")
     w = synth.WORKLOADS[args.workload]
-    st = workload_state(w, rank_seed(0, rank), device)
+    max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
+    st = workload_state(w, rank_seed(0, rank), device, max_tokens)
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -366,7 +387,8 @@ def run_ours(args, rank, world, local_rank):
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
         with open(tr_path) as f:
-            traffic = json.load(f).get(f"{args.workload}:{dom}")
+            key = args.workload + ("/batched" if max_tokens else "")
+            traffic = json.load(f).get(f"{key}:{dom}")
     cpu = cpu_baseline(w, tokens=args.cpu_tokens) if world == 1 and not args.no_cpu_baseline else None
     line = {
         "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
@@ -384,6 +406,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
                                f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
                    "tokens_per_step": w.T_valid, "parallelism": f"token-sharded replicas x{world}",
+                   "layout": (f"batched [{w.E + int(w.shared)}, {max_tokens}, H] + masked_m" if max_tokens
+                              else "contiguous expert-major rows + cu_seqlens"),
                    "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
         "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
         "kernels": kernels,
@@ -476,6 +500,11 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", choices=["contiguous", "batched"], default="contiguous",
+                    help="expert-major rows with cu_seqlens, or the batched [E, max_tokens, H] layout")
+    ap.add_argument("--max-tokens", type=int, default=0,
+                    help="rows per expert block of the batched layout (default: the bucket's T, which never "
+                         "overflows)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 MOE_BF16, MOE_E4M3 = 0, 1
 MOE_EPI_NONE, MOE_EPI_SWIGLU = 0, 1
-MOE_DEV_BAD_EXPERT, MOE_DEV_VERIFY_MISMATCH, MOE_DEV_PIPELINE_TIMEOUT = 1, 2, 4
+MOE_DEV_BAD_EXPERT, MOE_DEV_VERIFY_MISMATCH, MOE_DEV_PIPELINE_TIMEOUT, MOE_DEV_OVERFLOW = 1, 2, 4, 8
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_WORKSPACE", 3: "MOE_ERR_UNSUPPORTED", 4: "MOE_ERR_CUDA"}
 
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -29,7 +29,7 @@ class MoeError(RuntimeError):
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
-                ("weight_in_down", _I)]
+                ("weight_in_down", _I), ("max_tokens", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -39,7 +39,8 @@ class LayerWeights(ctypes.Structure):
 
 class LayerViews(ctypes.Structure):
     _fields_ = [("xp", _P), ("xp_scales", _P), ("hs", _P), ("hs_scales", _P), ("y", _P), ("cu_seqlens", _P),
-                ("src_row", _P), ("inv_map", _P), ("shared_map", _P), ("row_weights", _P), ("cap", _I)]
+                ("src_row", _P), ("inv_map", _P), ("shared_map", _P), ("row_weights", _P), ("cap", _I),
+                ("masked_m", _P)]
 
 
 # C signatures (restype int = moe_status_t unless noted)
@@ -52,11 +53,16 @@ _SIGS = {
     "moe_permute_noalloc_max_scratch_bytes": ([], _Z),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_permute_ex": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _P, _P, _P], _I),
+    "moe_permute_batched_workspace_bytes": ([_I, _I, _I, _I], _Z),
+    "moe_permute_batched": ([_P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _P, _P,
+                             _P], _I),
     "moe_amax_bf16": ([_P, _Z, _P, _P], _I),
     "moe_quantize_act_fp8": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_quantize_weight_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_ex": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gemm_batched": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P],
+                                 _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_combine_verify": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_combine_amax": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -164,6 +170,38 @@ def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, 
     return dict(xp=xp, xp_scales=xps, cu_seqlens=cu, src_row=src, inv_map=inv, shared_map=smap, row_weights=roww)
 
 
+def moe_permute_batched_workspace_bytes(T, K, E, with_shared):
+    return lib().moe_permute_batched_workspace_bytes(T, K, E, int(with_shared))
+
+
+def moe_permute_batched(topk_idx, E, x, max_tokens, with_shared=False, out_dtype=MOE_BF16, ws=None,
+                        dev_status=None, stream=None, dispatch_scale=None, topk_w=None):
+    """Batched layout: returns dict(xb [nseg, max_tokens, H], xb_scales, masked_m [nseg], src_row
+    [nseg * max_tokens], inv_map, shared_map, row_weights)."""
+    _dev(topk_idx)
+    _dev(x)
+    T, K = topk_idx.shape
+    H = x.shape[1]
+    dev = x.device
+    nseg = E + int(with_shared)
+    rows = nseg * max_tokens
+    fp8 = out_dtype == MOE_E4M3
+    xb = torch.empty(nseg, max_tokens, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    xbs = torch.empty(nseg, max_tokens, H // 128, dtype=torch.float32, device=dev) if fp8 else None
+    mm = torch.empty(nseg, dtype=torch.int32, device=dev)
+    src = torch.empty(rows, dtype=torch.int32, device=dev)
+    inv = torch.empty(T, K, dtype=torch.int32, device=dev)
+    smap = torch.empty(T, dtype=torch.int32, device=dev) if with_shared else None
+    roww = torch.empty(rows, dtype=torch.float32, device=dev) if topk_w is not None else None
+    if ws is None:
+        ws = torch.empty(moe_permute_batched_workspace_bytes(T, K, E, with_shared), dtype=torch.uint8, device=dev)
+    _check("moe_permute_batched", lib().moe_permute_batched(
+        _ptr(topk_idx), T, K, E, int(with_shared), max_tokens, _ptr(x), H, out_dtype, _ptr(xb), _ptr(xbs), _ptr(mm),
+        _ptr(src), _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _ptr(dispatch_scale), _ptr(topk_w), _ptr(roww), _stream(stream)))
+    return dict(xb=xb, xb_scales=xbs, masked_m=mm, src_row=src, inv_map=inv, shared_map=smap, row_weights=roww)
+
+
 def moe_quantize_act_fp8(x, stream=None):
     _dev(x)
     R, C = x.shape
@@ -214,6 +252,28 @@ def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=
     return out, out_scales
 
 
+def moe_grouped_gemm_batched(a, masked_m, w, a_scales=None, w_scales=None, w_extra=None, w_extra_scales=None,
+                             epilogue=MOE_EPI_NONE, out=None, out_scales=None, dev_status=None, stream=None,
+                             row_scale=None):
+    """a [S, max_tokens, k] (bf16 or uint8 E4M3 codes), masked_m int32 [S]; w [num_w, n, k];
+    returns (out [S, max_tokens, n_out], out_scales)."""
+    _dev(a)
+    fp8 = a.dtype == torch.uint8
+    S, max_tokens, k_dim = a.shape
+    num_w, n_dim = w.shape[0], w.shape[1]
+    out_cols = n_dim // 2 if epilogue == MOE_EPI_SWIGLU else n_dim
+    if out is None:
+        odt = torch.uint8 if (fp8 and epilogue == MOE_EPI_SWIGLU) else torch.bfloat16
+        out = torch.empty(S, max_tokens, out_cols, dtype=odt, device=a.device)
+    if fp8 and epilogue == MOE_EPI_SWIGLU and out_scales is None:
+        out_scales = torch.empty(S, max_tokens, out_cols // 128, dtype=torch.float32, device=a.device)
+    _check("moe_grouped_gemm_batched", lib().moe_grouped_gemm_batched(
+        _ptr(a), _ptr(a_scales), _ptr(masked_m), S, max_tokens, k_dim, n_dim, _ptr(w), _ptr(w_scales), num_w,
+        _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out), _ptr(out_scales),
+        _ptr(dev_status), _ptr(row_scale), _stream(stream)))
+    return out, out_scales
+
+
 def moe_combine(y, inv_map, topk_w, shared_y=None, shared_map=None, fq_scale=None, out=None, stream=None):
     _dev(y)
     T, K = inv_map.shape
@@ -261,8 +321,9 @@ class MoeLayer:
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
-                 weight_in_down=False):
-        self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down))
+                 weight_in_down=False, max_tokens=0):
+        self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
+                              int(max_tokens))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

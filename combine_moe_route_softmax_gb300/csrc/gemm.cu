@@ -71,7 +71,8 @@ struct SmemLayout {
 constexpr size_t SMEM_BYTES = SmemLayout::end + 1024;           // + alignment slack
 
 struct Args {
-  const int32_t* cu;
+  const int32_t* cu;        // cu_seqlens [nseg + 1], or masked_m [nseg] when max_tokens > 0
+  int max_tokens;           // 0: contiguous segments; > 0: segment s owns rows [s*max_tokens, ...)
   int nseg;
   int rows_cap;
   int k_dim;
@@ -229,7 +230,16 @@ __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __e
 struct Unit {
   int seg, row0, row_end, nt;
 };
-__device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, const int* prefix, int nseg) {
+// Segment bounds kept in shared memory as bnd[]: contiguous segments [bnd[s], bnd[s+1]);
+// batched segments [s*max_tokens, bnd[s]) (bnd[s] = the segment's end row).
+__device__ __forceinline__ int seg_begin(const int* bnd, int s, int max_tokens) {
+  return max_tokens > 0 ? s * max_tokens : bnd[s];
+}
+__device__ __forceinline__ int seg_end(const int* bnd, int s, int max_tokens) {
+  return max_tokens > 0 ? bnd[s] : bnd[s + 1];
+}
+__device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, const int* prefix, int nseg,
+                                            int max_tokens) {
   Unit w;
   const int mt = u / n_tiles;
   w.nt = u - mt * n_tiles;
@@ -242,8 +252,8 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, c
       hi = mid - 1;
   }
   w.seg = lo;
-  w.row0 = cu[lo] + (mt - prefix[lo]) * BM;
-  w.row_end = cu[lo + 1];
+  w.row0 = seg_begin(cu, lo, max_tokens) + (mt - prefix[lo]) * BM;
+  w.row_end = seg_end(cu, lo, max_tokens);
   return w;
 }
 
@@ -271,7 +281,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* stage_out = smem + SmemLayout::stage_out;
 
   const int nseg = args.nseg;
-  for (int i = tid; i <= nseg; i += THREADS) cu_s[i] = args.cu[i];
+  const int mtok = args.max_tokens;
+  if (mtok > 0) {
+    for (int i = tid; i < nseg; i += THREADS) cu_s[i] = i * mtok + min(max(args.cu[i], 0), mtok);
+  } else {
+    for (int i = tid; i <= nseg; i += THREADS) cu_s[i] = args.cu[i];
+  }
   if (tid == 64) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);
@@ -296,7 +311,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int chunk = (nseg + 31) / 32;
     const int s0 = min(nseg, lane * chunk), s1 = min(nseg, s0 + chunk);
     int local = 0;
-    for (int s = s0; s < s1; ++s) local += (max(0, cu_s[s + 1] - cu_s[s]) + BM - 1) / BM;
+    auto len = [&](int s) { return max(0, seg_end(cu_s, s, mtok) - seg_begin(cu_s, s, mtok)); };
+    for (int s = s0; s < s1; ++s) local += (len(s) + BM - 1) / BM;
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -306,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int run = incl - local;
     for (int s = s0; s < s1; ++s) {
       prefix[s] = run;
-      run += (max(0, cu_s[s + 1] - cu_s[s]) + BM - 1) / BM;
+      run += (len(s) + BM - 1) / BM;
     }
     if (lane == 31) prefix[nseg] = incl;
   }
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg);
+        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
         const bool extra = w.seg >= args.num_w;
         const CUtensorMap* mb = extra ? &tmBx : &tmB;
         const int wbase = extra ? 0 : w.seg * args.n_dim;
@@ -443,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t tphase = 0;
     const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg);
+      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
       const int row = w.row0 + r_in_tile;
       const bool row_ok = row < w.row_end;
       // first output column this thread covers and whether that 128-column block exists
@@ -678,14 +694,15 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMa
 }  // namespace gg
 }  // namespace moe
 
-extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int32_t* cu_seqlens,
-                                            int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
-                                            const float* w_scales, int num_w, const void* w_extra,
-                                            const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
-                                            void* out, float* out_scales, int32_t* dev_status,
-                                            const float* row_scale, void* stream) {
-  using namespace moe;
-  using namespace moe::gg;
+namespace moe {
+namespace gg {
+// max_tokens == 0: segments from cu_seqlens over rows_cap rows; > 0: batched segments
+// (bounds = masked_m) over rows_cap = num_segments * max_tokens rows.
+static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_t* cu_seqlens, int max_tokens,
+                              int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
+                              const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
+                              moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
+                              int32_t* dev_status, const float* row_scale, void* stream) {
   const bool fp8 = dtype == MOE_E4M3;
   const bool swiglu = epilogue == MOE_EPI_SWIGLU;
   if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -716,6 +733,7 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
   }
   Args args;
   args.cu = cu_seqlens;
+  args.max_tokens = max_tokens;
   args.nseg = num_segments;
   args.rows_cap = rows_cap;
   args.k_dim = k_dim;
@@ -737,6 +755,30 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
   if (fp8)
     return swiglu ? launch<true, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<true, false>(ma, mb, mbx, mah, args, grid, pair, s);
   return swiglu ? launch<false, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<false, false>(ma, mb, mbx, mah, args, grid, pair, s);
+}
+}  // namespace gg
+}  // namespace moe
+
+extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int32_t* cu_seqlens,
+                                            int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
+                                            const float* w_scales, int num_w, const void* w_extra,
+                                            const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
+                                            void* out, float* out_scales, int32_t* dev_status,
+                                            const float* row_scale, void* stream) {
+  return moe::gg::gemm_impl(a, a_scales, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
+                            w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_batched(const void* a, const float* a_scales, const int32_t* masked_m,
+                                                 int num_segments, int max_tokens, int k_dim, int n_dim,
+                                                 const void* w, const float* w_scales, int num_w,
+                                                 const void* w_extra, const float* w_extra_scales, moe_dtype_t dtype,
+                                                 moe_epilogue_t epilogue, void* out, float* out_scales,
+                                                 int32_t* dev_status, const float* row_scale, void* stream) {
+  if (max_tokens < 1 || num_segments < 0 || (long long)num_segments * max_tokens > 0x7fffffffll) return MOE_ERR_ARG;
+  return moe::gg::gemm_impl(a, a_scales, masked_m, max_tokens, num_segments, num_segments * max_tokens, k_dim,
+                            n_dim, w, w_scales, num_w, w_extra, w_extra_scales, dtype, epilogue, out, out_scales,
+                            dev_status, row_scale, stream);
 }
 
 extern "C" moe_status_t moe_grouped_gemm(const void* a, const float* a_scales, const int32_t* cu_seqlens,

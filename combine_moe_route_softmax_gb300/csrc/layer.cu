@@ -8,7 +8,9 @@
 // page's rule -- every region 256-byte aligned):
 //   cu_seqlens [E+2] | src_row [cap] | inv_map [T*K] | shared_map [T] | permute scratch |
 //   xp [cap, H] (+ scales [cap, H/128]) | hs [cap, I] (+ scales [cap, I/128]) | y [cap, H] bf16
-// with cap = T*K + (has_shared ? T : 0).
+// with cap = T*K + (has_shared ? T : 0).  The batched layout (max_tokens > 0) has
+// cap = (E + has_shared) * max_tokens rows, masked_m [E+1] in place of cu_seqlens, and the
+// batched permute's scratch (which keeps its cu_seqlens internal).
 #include "common.cuh"
 
 namespace moe {
@@ -25,17 +27,20 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
   if (!d) return false;
   if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E < 1 || d->E > kMaxExperts || d->K < 1 || d->K > d->E ||
       d->K > kMaxTopK || d->H % 128 || d->I % 128 || (d->has_shared != 0 && d->has_shared != 1) ||
-      (d->weight_in_down != 0 && d->weight_in_down != 1) ||
+      (d->weight_in_down != 0 && d->weight_in_down != 1) || d->max_tokens < 0 ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
-  const size_t cap = T * K + (d->has_shared ? T : 0);
-  if (cap > 0x7fffffffull) return false;
+  const bool batched = d->max_tokens > 0;
+  const size_t nseg = (size_t)d->E + d->has_shared;
+  const size_t cap = batched ? nseg * (size_t)d->max_tokens : T * K + (d->has_shared ? T : 0);
+  if (cap > 0x7fffffffull || T * K + T > 0x7fffffffull) return false;
   const size_t esz = d->dtype == MOE_E4M3 ? 1 : 2;
   const bool fp8 = d->dtype == MOE_E4M3;
   p->cap = (int)cap;
-  p->nseg = d->E + d->has_shared;
-  p->scratch_bytes = moe_permute_workspace_bytes(d->T, d->K, d->E, d->has_shared);
+  p->nseg = (int)nseg;
+  p->scratch_bytes = batched ? moe_permute_batched_workspace_bytes(d->T, d->K, d->E, d->has_shared)
+                             : moe_permute_workspace_bytes(d->T, d->K, d->E, d->has_shared);
   size_t o = 0;
   p->off_cu = o;      o = align256(o + 4 * (size_t)(p->nseg + 1));
   p->off_src = o;     o = align256(o + 4 * cap);
@@ -64,7 +69,10 @@ extern "C" moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe
   if (!moe::plan_layer(d, &p) || !ws || !v) return MOE_ERR_ARG;
   uint8_t* b = static_cast<uint8_t*>(ws);
   const bool fp8 = d->dtype == MOE_E4M3;
-  v->cu_seqlens = reinterpret_cast<int32_t*>(b + p.off_cu);
+  const bool batched = d->max_tokens > 0;
+  // one region: cu_seqlens [nseg + 1] in the contiguous layout, masked_m [nseg] in the batched
+  v->cu_seqlens = batched ? nullptr : reinterpret_cast<int32_t*>(b + p.off_cu);
+  v->masked_m = batched ? reinterpret_cast<int32_t*>(b + p.off_cu) : nullptr;
   v->src_row = reinterpret_cast<int32_t*>(b + p.off_src);
   v->inv_map = reinterpret_cast<int32_t*>(b + p.off_inv);
   v->shared_map = d->has_shared ? reinterpret_cast<int32_t*>(b + p.off_smap) : nullptr;
@@ -104,13 +112,34 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
     if (st != MOE_OK) return st;
   }
   const bool wd = d->weight_in_down != 0;
+  const void* sx13 = d->has_shared ? w->shared_w13 : nullptr;
+  const void* sx2 = d->has_shared ? w->shared_w2 : nullptr;
+  const float* sx13s = d->has_shared ? w->shared_w13_scales : nullptr;
+  const float* sx2s = d->has_shared ? w->shared_w2_scales : nullptr;
+  if (d->max_tokens > 0) {
+    // batched layout: same steps, segment s in rows [s*max_tokens, s*max_tokens + masked_m[s])
+    const int mt = d->max_tokens;
+    st = moe_permute_batched(topk_idx, d->T, d->K, d->E, d->has_shared, mt, x, d->H, d->dtype, v.xp, v.xp_scales,
+                             v.masked_m, v.src_row, v.inv_map, v.shared_map,
+                             static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes, dev_status,
+                             dispatch_scale, wd ? topk_w : nullptr, wd ? v.row_weights : nullptr, stream);
+    if (st != MOE_OK) return st;
+    st = moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, p.nseg, mt, d->H, 2 * d->I, w->w13,
+                                  w->w13_scales, d->E, sx13, sx13s, d->dtype, MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                  dev_status, nullptr, stream);
+    if (st != MOE_OK) return st;
+    st = moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, p.nseg, mt, d->I, d->H, w->w2, w->w2_scales,
+                                  d->E, sx2, sx2s, d->dtype, MOE_EPI_NONE, v.y, nullptr, dev_status,
+                                  wd ? v.row_weights : nullptr, stream);
+    if (st != MOE_OK) return st;
+    return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
+                       v.shared_map, fq_scale, out, stream);
+  }
   st = moe_permute_ex(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales,
                       v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch,
                       p.scratch_bytes, dev_status, dispatch_scale, wd ? topk_w : nullptr,
                       wd ? v.row_weights : nullptr, stream);
   if (st != MOE_OK) return st;
-  const void* sx13 = d->has_shared ? w->shared_w13 : nullptr;
-  const void* sx2 = d->has_shared ? w->shared_w2 : nullptr;
   st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
                         sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
                         v.hs_scales, dev_status, stream);

@@ -15,6 +15,8 @@
 //           into cu_seqlens
 //   scatter per-block: per-warp histograms, a warp-level scan, then an ordered walk with
 //           __match_any_sync ranks -> src_row / inv_map / shared_map (stable by slot)
+//           (batched layout: the row of rank r in segment e goes to e*max_tokens + r,
+//           ranks past max_tokens are dropped, and masked_m[e] = min(count, max_tokens))
 //   gather  source-ordered: one warp per token reads its row once (16-byte loads) and
 //           writes it to every row that holds it (the token's slots and its shared row),
 //           as BF16 or as E4M3 codes + 1x128 scales.  HBM-bound:
@@ -137,7 +139,8 @@ __global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__
 __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     const int32_t* __restrict__ idx, int T, int K, int E, int with_shared, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ cu_seqlens, int cap, int32_t* __restrict__ src_row, int32_t* __restrict__ inv_map,
-    int32_t* __restrict__ shared_map, const float* __restrict__ topk_w, float* __restrict__ row_w) {
+    int32_t* __restrict__ shared_map, const float* __restrict__ topk_w, float* __restrict__ row_w, int max_tokens,
+    int32_t* __restrict__ masked_m, int32_t* dev_status) {
   extern __shared__ int whist[];  // [kPermWarps][nseg]
   const int nseg = E + with_shared;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -162,8 +165,10 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
   }
   __syncthreads();
   // 2. each warp's starting row per segment = block offset + earlier warps' counts
+  // (batched layout: rows counted from the segment's block e*max_tokens)
+  const bool batched = max_tokens > 0;
   for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
-    int run = cu_seqlens[e] + offsets[(size_t)e * gridDim.x + blockIdx.x];
+    int run = (batched ? e * max_tokens : cu_seqlens[e]) + offsets[(size_t)e * gridDim.x + blockIdx.x];
     for (int w = 0; w < kPermWarps; ++w) {
       const int c = whist[w * nseg + e];
       whist[w * nseg + e] = run;
@@ -182,9 +187,13 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     if (ok) {
       rank = __popc(peers & lanemask_lt());
       const int pos = my[e] + rank;
-      src_row[pos] = s;
-      if (row_w) row_w[pos] = topk_w[s];
-      inv_map[s] = pos;
+      if (batched && pos - e * max_tokens >= max_tokens) {
+        inv_map[s] = -1;   // past the segment's block: dropped (flagged below, per segment)
+      } else {
+        src_row[pos] = s;
+        if (row_w) row_w[pos] = topk_w[s];
+        inv_map[s] = pos;
+      }
     } else if (inr) {
       inv_map[s] = -1;
     }
@@ -202,9 +211,13 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
       const unsigned ball = __ballot_sync(0xffffffffu, any);
       if (any) {
         const int pos = my[E] + __popc(ball & lanemask_lt());
-        src_row[pos] = T * K + t;
-        if (row_w) row_w[pos] = 1.0f;
-        shared_map[t] = pos;
+        if (batched && pos - E * max_tokens >= max_tokens) {
+          shared_map[t] = -1;
+        } else {
+          src_row[pos] = T * K + t;
+          if (row_w) row_w[pos] = 1.0f;
+          shared_map[t] = pos;
+        }
       } else if (inr) {
         shared_map[t] = -1;
       }
@@ -213,10 +226,28 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
       __syncwarp();
     }
   }
-  // rows past the last one: -1
-  const int total = cu_seqlens[nseg];
-  for (int p = total + blockIdx.x * blockDim.x + threadIdx.x; p < cap; p += gridDim.x * blockDim.x)
-    src_row[p] = -1;
+  if (!batched) {
+    // rows past the last one: -1
+    const int total = cu_seqlens[nseg];
+    for (int p = total + blockIdx.x * blockDim.x + threadIdx.x; p < cap; p += gridDim.x * blockDim.x)
+      src_row[p] = -1;
+    return;
+  }
+  // batched: masked_m, the overflow flag, and -1 in every row of a block past its masked_m
+  // (disjoint from the rows written above, so no ordering between blocks is needed)
+  if (blockIdx.x == 0) {
+    bool over = false;
+    for (int e = threadIdx.x; e < nseg; e += blockDim.x) {
+      const int c = cu_seqlens[e + 1] - cu_seqlens[e];
+      masked_m[e] = min(c, max_tokens);
+      over |= c > max_tokens;
+    }
+    if (over && dev_status) atomicOr(dev_status, MOE_DEV_OVERFLOW);
+  }
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < cap; p += gridDim.x * blockDim.x) {
+    const int e = p / max_tokens;
+    if (p - e * max_tokens >= cu_seqlens[e + 1] - cu_seqlens[e]) src_row[p] = -1;
+  }
 }
 
 // Destination rows of token t: its valid slots' rows (inv_map) and its shared row.  Lane
@@ -397,20 +428,38 @@ extern "C" size_t moe_permute_workspace_bytes(int T, int K, int E, int with_shar
   return scratch_layout(perm_blocks(T), nseg).total;
 }
 
+extern "C" size_t moe_permute_batched_workspace_bytes(int T, int K, int E, int with_shared) {
+  // the contiguous scratch plus the segments' cu_seqlens, which the batched layout keeps
+  // internal (its callers get masked_m)
+  const size_t b = moe_permute_workspace_bytes(T, K, E, with_shared);
+  if (b == 0) return 0;
+  const size_t nseg = (size_t)E + (with_shared ? 1 : 0);
+  return b + (nseg + 1) * sizeof(int32_t) + 255 - ((nseg + 1) * sizeof(int32_t) + 255) % 256;
+}
+
 namespace moe {
 static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with_shared, const uint16_t* x,
                                  int H, moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens,
                                  int32_t* src_row, int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, const float* dq_scale, const float* topk_w, float* row_w,
-                                 void* stream) {
+                                 int max_tokens, int32_t* masked_m, void* stream) {
   if (T < 0 || K < 1 || K > kMaxTopK || E < 1 || E > kMaxExperts || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
   if (with_shared != 0 && with_shared != 1) return MOE_ERR_ARG;
   if (out_dtype != MOE_BF16 && out_dtype != MOE_E4M3) return MOE_ERR_ARG;
-  if (!cu_seqlens) return MOE_ERR_ARG;
+  const bool batched = max_tokens != 0;
   const int nseg = E + with_shared;
+  if (batched) {
+    if (max_tokens < 0 || (size_t)nseg * max_tokens > 0x7fffffffull || !masked_m) return MOE_ERR_ARG;
+  } else if (!cu_seqlens) {
+    return MOE_ERR_ARG;
+  }
   cudaStream_t s = as_stream(stream);
   if (T == 0) {
-    if (cudaMemsetAsync(cu_seqlens, 0, sizeof(int32_t) * (nseg + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t* z = batched ? masked_m : cu_seqlens;
+    if (cudaMemsetAsync(z, 0, sizeof(int32_t) * (batched ? nseg : nseg + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (batched && src_row &&
+        cudaMemsetAsync(src_row, 0xff, sizeof(int32_t) * (size_t)nseg * max_tokens, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     return MOE_OK;
   }
   if (!topk_idx || !x || !xp || !src_row || !inv_map || (with_shared && !shared_map)) return MOE_ERR_ARG;
@@ -419,7 +468,8 @@ static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, i
   if (row_w && !topk_w) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xp)) & 15) return MOE_ERR_ARG;
   if ((size_t)T * K + T > 0x7fffffffull) return MOE_ERR_ARG;
-  const size_t need = moe_permute_workspace_bytes(T, K, E, with_shared);
+  const size_t need = batched ? moe_permute_batched_workspace_bytes(T, K, E, with_shared)
+                              : moe_permute_workspace_bytes(T, K, E, with_shared);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
   const int nblk = perm_blocks(T);
   const ScratchLayout lay = scratch_layout(nblk, nseg);
@@ -427,7 +477,8 @@ static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, i
   int32_t* counts = reinterpret_cast<int32_t*>(base + lay.counts);
   int32_t* seg_total = reinterpret_cast<int32_t*>(base + lay.seg_total);
   int32_t* ticket = reinterpret_cast<int32_t*>(base + lay.ticket);
-  const int cap = T * K + (with_shared ? T : 0);
+  if (batched) cu_seqlens = reinterpret_cast<int32_t*>(base + lay.total);
+  const int cap = batched ? nseg * max_tokens : T * K + (with_shared ? T : 0);
   permute_count_kernel<<<nblk, kPermThreads, nseg * sizeof(int), s>>>(topk_idx, T, K, E, with_shared, counts,
                                                                         ticket, dev_status);
   MOE_CHECK_LAUNCH();
@@ -441,7 +492,8 @@ static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, i
   }
   permute_scatter_kernel<<<nblk, kPermThreads, scatter_smem, s>>>(topk_idx, T, K, E, with_shared, counts,
                                                                   cu_seqlens, cap, src_row, inv_map, shared_map,
-                                                                  topk_w, row_w);
+                                                                  topk_w, row_w, batched ? max_tokens : 0,
+                                                                  masked_m, dev_status);
   MOE_CHECK_LAUNCH();
   const int gblocks = min((T + 7) / 8, num_sms() * 8);
   const int32_t* smap = with_shared ? shared_map : nullptr;
@@ -466,7 +518,8 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
                                     int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
                                     void* stream) {
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
-                           inv_map, shared_map, ws, ws_bytes, dev_status, nullptr, nullptr, nullptr, stream);
+                           inv_map, shared_map, ws, ws_bytes, dev_status, nullptr, nullptr, nullptr, 0, nullptr,
+                           stream);
 }
 
 extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, int E, int with_shared,
@@ -476,8 +529,20 @@ extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, in
                                        const float* dispatch_scale, const float* topk_w, float* row_weights,
                                        void* stream) {
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
+                           inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights, 0,
+                           nullptr, stream);
+}
+
+extern "C" moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                            int max_tokens, const uint16_t* x, int H, moe_dtype_t out_dtype,
+                                            void* xb, float* xb_scales, int32_t* masked_m, int32_t* src_row,
+                                            int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
+                                            int32_t* dev_status, const float* dispatch_scale,
+                                            const float* topk_w, float* row_weights, void* stream) {
+  if (max_tokens < 1) return MOE_ERR_ARG;
+  return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xb, xb_scales, nullptr, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights,
-                           stream);
+                           max_tokens, masked_m, stream);
 }
 
 extern "C" moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,

@@ -53,9 +53,11 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 #define MOE_DEV_BAD_EXPERT 1        /* an expert id outside [-1, E): slot treated as padding */
 #define MOE_DEV_VERIFY_MISMATCH 2   /* moe_combine_verify found an element that differs */
 #define MOE_DEV_PIPELINE_TIMEOUT 4  /* a GEMM pipeline wait gave up; its output is invalid */
+#define MOE_DEV_OVERFLOW 8          /* batched layout: a segment received more than max_tokens
+                                       rows; the slots past max_tokens were dropped */
 
 /* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
- * dispatch fake-quant options). */
+ * dispatch fake-quant options, 3 the batched expert layout). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -214,6 +216,52 @@ moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int
                                  moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
                                  int32_t* dev_status, const float* row_scale, void* stream);
 
+/* ------------------------------------------------------------ batched expert layout
+ * The expert-batched activation format ([DeepEP]: the low-latency dispatch hands the
+ * experts one fixed block of rows per expert, 3-D [E, max_tokens, H], while the
+ * high-throughput dispatch produces the 2-D contiguous layout above; the experts' kernel has
+ * to know which format it gets).  Segment s owns rows [s*max_tokens, (s+1)*max_tokens) of
+ * a [nseg * max_tokens, H] buffer; its first masked_m[s] rows are real, the rest padding
+ * that no call reads or writes.
+ *
+ * moe_permute_batched: the same stable counting sort as moe_permute (segment e holds the
+ * slots with topk_idx == e in ascending flat index s = t*K + k; segment E the shared rows
+ * of with_shared, ascending t), with the row of rank r in segment e at e*max_tokens + r.
+ *   max_tokens >= 1; (E + with_shared) * max_tokens < 2^31.
+ *   xb         [nseg * max_tokens, H]: BF16 copies, or E4M3 codes with xb_scales float32
+ *              [nseg * max_tokens, H/128] (the 1x128 rule of moe_permute).
+ *   masked_m   out int32 [nseg]: min(rows of segment e, max_tokens).
+ *   src_row    out int32 [nseg * max_tokens]: source index of each real row, -1 elsewhere.
+ *   inv_map    out int32 [T, K]: row of each slot; -1 for padding and for dropped slots.
+ *   shared_map out int32 [T] (iff with_shared): the token's shared row, or -1.
+ *   A segment with more than max_tokens rows keeps its first max_tokens (lowest flat
+ *   index) and drops the rest: their inv_map / shared_map entries are -1 and
+ *   MOE_DEV_OVERFLOW is ORed into dev_status.  (With distinct experts per token a segment
+ *   holds at most T rows, so max_tokens >= T never drops.)
+ *   ws         at least moe_permute_batched_workspace_bytes(T, K, E, with_shared) bytes.
+ *   dispatch_scale, topk_w, row_weights: as moe_permute_ex (row_weights [nseg*max_tokens]).
+ * Errors: as moe_permute_ex. */
+size_t moe_permute_batched_workspace_bytes(int T, int K, int E, int with_shared);
+moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int K, int E, int with_shared,
+                                 int max_tokens, const uint16_t* x, int H, moe_dtype_t out_dtype, void* xb,
+                                 float* xb_scales, int32_t* masked_m, int32_t* src_row, int32_t* inv_map,
+                                 int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                 const float* dispatch_scale, const float* topk_w, float* row_weights,
+                                 void* stream);
+
+/* moe_grouped_gemm_ex over the batched layout: segment s covers rows
+ * [s*max_tokens, s*max_tokens + min(max(masked_m[s], 0), max_tokens)) of a, out,
+ * a_scales, out_scales and row_scale, all with nseg * max_tokens rows; masked_m is int32
+ * [num_segments] on the device (read by the kernel: no host synchronisation).  Every other
+ * argument, the arithmetic and the errors are those of moe_grouped_gemm_ex; rows past a
+ * segment's masked_m are neither read into a result nor written. */
+moe_status_t moe_grouped_gemm_batched(const void* a, const float* a_scales, const int32_t* masked_m,
+                                      int num_segments, int max_tokens, int k_dim, int n_dim, const void* w,
+                                      const float* w_scales, int num_w, const void* w_extra,
+                                      const float* w_extra_scales, moe_dtype_t dtype, moe_epilogue_t epilogue,
+                                      void* out, float* out_scales, int32_t* dev_status,
+                                      const float* row_scale, void* stream);
+
 /* -------------------------------------------------------------------------- combine
  * Fixed-order combine ([MegaMoE]: each token's router-weighted slot rows are added in
  * increasing slot order into a float32 accumulator that starts at zero, rounded to BF16
@@ -272,6 +320,9 @@ typedef struct {
   int has_shared;     /* 1: one shared expert, added last in the combine, never quantised */
   int weight_in_down; /* 1: router weights applied in the down projection's epilogue (rows
                          stored weighted in BF16, the combine only sums); 0: in the combine */
+  int max_tokens;     /* 0: contiguous expert-major layout (cu_seqlens); > 0: the batched
+                         layout, max_tokens rows per segment (the shared expert's included),
+                         through moe_permute_batched / moe_grouped_gemm_batched (ABI 3) */
 } moe_layer_desc_t;
 
 typedef struct {
@@ -295,7 +346,9 @@ typedef struct {
   int32_t* inv_map;             /* [T, K] */
   int32_t* shared_map;          /* [T] or NULL */
   float* row_weights;           /* [cap] router weight per row (weight_in_down) */
-  int cap;                      /* T*K + (has_shared ? T : 0) */
+  int cap;                      /* T*K + (has_shared ? T : 0); batched: nseg * max_tokens */
+  int32_t* masked_m;            /* batched layout: [E + has_shared] rows per segment; else NULL
+                                   (and cu_seqlens is NULL in the batched layout) */
 } moe_layer_views_t;
 
 /* Workspace bytes for a layer of this shape (0 for an invalid descriptor). */

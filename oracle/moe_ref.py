@@ -16,6 +16,7 @@ from .formats import (bf16_bits_to_f32, e4m3_decode, e4m3_encode, f32_to_bf16_bi
 F32 = np.float32
 STATUS_BAD_EXPERT = 1
 STATUS_VERIFY_MISMATCH = 2
+STATUS_OVERFLOW = 8
 
 
 # ----------------------------------------------------------------------------- route
@@ -97,6 +98,58 @@ def permute(topk_idx, E, with_shared=False):
         shared_map = np.full(T, -1, dtype=np.int32)
         shared_map[src_row[n_routed:n_total] - T * K] = np.arange(n_routed, n_total, dtype=np.int32)
     return cu, src_row, inv_map.reshape(T, K), shared_map, status
+
+
+def permute_batched(topk_idx, E, max_tokens, with_shared=False):
+    """The expert-batched layout of the DeepEP page: each expert gets a fixed block of
+    max_tokens rows ([E, max_tokens, H], 3-D) plus the number of rows it really received,
+    where the high-throughput path uses the contiguous 2-D layout.
+
+    The page does not fix the order of the rows inside a block; this takes the order of
+    the contiguous layout: block e lists, in ascending flat slot s = t*K + k, the slots with
+    topk_idx == e, so its row r is the r-th such slot.  With with_shared, block E lists
+    the tokens that have a valid slot, ascending t, source index T*K + t.  A block keeps
+    its first max_tokens entries; the others are dropped (no row, inv_map / shared_map -1)
+    and set the overflow bit of the status word.  An id outside [-1, E) is padding with
+    the bad-expert bit, as in the contiguous permute.
+
+    Returns masked_m [nseg] (rows kept per block), src_row [nseg * max_tokens] (source of
+    each row, -1 for unused rows), inv_map [T, K], shared_map [T] (None without
+    with_shared) and the status word.
+    """
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    T, K = idx.shape
+    nseg = E + (1 if with_shared else 0)
+    status = 0
+    blocks = [[] for _ in range(nseg)]
+    for t in range(T):
+        for k in range(K):
+            e = int(idx[t, k])
+            if e == -1:
+                continue
+            if e < -1 or e >= E:
+                status |= STATUS_BAD_EXPERT
+                continue
+            blocks[e].append(t * K + k)
+    if with_shared:
+        blocks[E] = [T * K + t for t in range(T) if any(0 <= int(e) < E for e in idx[t])]
+    masked_m = np.zeros(nseg, dtype=np.int32)
+    src_row = np.full(nseg * max_tokens, -1, dtype=np.int32)
+    inv_map = np.full((T, K), -1, dtype=np.int32)
+    shared_map = np.full(T, -1, dtype=np.int32) if with_shared else None
+    for b, entries in enumerate(blocks):
+        if len(entries) > max_tokens:
+            status |= STATUS_OVERFLOW
+        kept = entries[:max_tokens]
+        masked_m[b] = len(kept)
+        for r, src in enumerate(kept):
+            row = b * max_tokens + r
+            src_row[row] = src
+            if src < T * K:
+                inv_map[src // K, src % K] = row
+            else:
+                shared_map[src - T * K] = row
+    return masked_m, src_row, inv_map, shared_map, status
 
 
 def row_tokens(src_row, T, K):

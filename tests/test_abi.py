@@ -39,13 +39,16 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_host_only_calls(lib):
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
     assert lib.moe_status_string(2) == b"workspace too small"
     # scratch sized from the inputs: grows with T, K and E
     a = lib.moe_permute_workspace_bytes(128, 8, 256, 1)
     b = lib.moe_permute_workspace_bytes(16384, 8, 256, 1)
     assert 0 < a < b and b % 256 == 0
     assert lib.moe_permute_workspace_bytes(16, 2, 0, 0) == 0
+    # the batched layout keeps its cu_seqlens in the scratch: one more 256-byte-aligned region
+    c = lib.moe_permute_batched_workspace_bytes(128, 8, 256, 1)
+    assert c == a + 1280 and lib.moe_permute_batched_workspace_bytes(16, 2, 0, 0) == 0
 
 
 def test_layer_workspace_size(lib):
@@ -55,6 +58,17 @@ def test_layer_workspace_size(lib):
     assert n >= cap * 7168 * 2 * 2 + cap * 2048 * 2
     bad = moe.LayerDesc(16, 100, 2048, 8, 2, moe.MOE_BF16, 0)   # H not a multiple of 128
     assert lib.moe_layer_workspace_bytes(ctypes.byref(bad)) == 0
+    # batched layout: (E + 1) blocks of max_tokens rows instead of T*K + T rows
+    db = moe.LayerDesc(128, 7168, 2048, 256, 8, moe.MOE_E4M3, 1, 0, 128)
+    nb = lib.moe_layer_workspace_bytes(ctypes.byref(db))
+    assert nb >= 257 * 128 * (7168 + 2048 + 7168 * 2)
+    views = moe.LayerViews()
+    assert lib.moe_layer_views(ctypes.byref(db), 1 << 20, ctypes.byref(views)) == 0
+    assert views.cap == 257 * 128 and views.cu_seqlens is None and views.masked_m == 1 << 20
+    db.max_tokens = -1
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(db)) == 0
+    db.max_tokens = 1 << 24   # 257 blocks of 2^24 rows: more than 2^31 rows
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(db)) == 0
 
 
 def test_argument_errors_launch_nothing(lib):
@@ -65,3 +79,10 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.moe_grouped_gemm(None, None, None, 1, 16, 100, 256, None, None, 1, None, None, 0, 0, None, None,
                                 None, None) == 1
     assert lib.moe_combine(None, None, None, 4, 2, 100, None, None, None, None, None) == 1
+    # batched layout: max_tokens < 1, or more than 2^31 rows
+    assert lib.moe_permute_batched(None, 4, 2, 8, 0, 0, None, 128, 0, None, None, None, None, None, None, None, 0,
+                                   None, None, None, None, None) == 1
+    assert lib.moe_grouped_gemm_batched(None, None, None, 1, 0, 128, 256, None, None, 1, None, None, 0, 0, None,
+                                        None, None, None, None) == 1
+    assert lib.moe_grouped_gemm_batched(None, None, None, 1025, 1 << 22, 128, 256, None, None, 1025, None, None, 0,
+                                        0, None, None, None, None, None) == 1

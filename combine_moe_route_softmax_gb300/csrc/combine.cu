@@ -15,28 +15,38 @@
 // __fdiv_rn) so the compiler cannot contract them into FMAs: the result is bit-exact
 // against a float32 reference fed the same rows.
 //
-// One warp per token; lane l owns 16-byte vectors l, l+32, ... of the H columns.  For
-// each vector, the K slot rows are loaded together (up to 8 16-byte loads in flight per
-// lane) before the ordered sum.  HBM-bound: N*H*2 + N_shared*H*2 read, T*H*2 written.
+// One warp per (token, column part); lane l owns 16-byte vectors l, l+32, ... of the
+// part.  A token's row is split into `splits` parts only when there are too few tokens
+// to fill the GPU (decode: 128 tokens); the order of the sum is per element, so the split
+// changes nothing in the result.  For each vector, the K slot rows are loaded together
+// (up to 8 16-byte loads in flight per lane) before the ordered sum.  HBM-bound:
+// N*H*2 + N_shared*H*2 read, T*H*2 written.
 #include "common.cuh"
 
 namespace moe {
 
 enum CombineMode { kWrite = 0, kVerify = 1, kAmax = 2 };
 
-template <int MODE, bool FQ, int KMAX>
+// K <= 8: at most 64 registers, so 4 blocks (32 warps) per SM keep enough loads in flight.
+// SPLIT = false (enough tokens) is the plain warp-per-token loop.
+template <int MODE, bool FQ, int KMAX, bool SPLIT>
 __global__ void __launch_bounds__(256) combine_kernel(
     const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_map, const float* __restrict__ topk_w, int T,
     int K, int H, const uint16_t* __restrict__ shared_y, const int32_t* __restrict__ shared_map,
     const float* __restrict__ fq_scale, uint16_t* __restrict__ out, const uint16_t* __restrict__ expected,
-    int32_t* dev_status, float* amax_out) {
+    int32_t* dev_status, float* amax_out, int splits) {
   const int lane = threadIdx.x & 31;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / 8;
+  const int per_part = SPLIT ? (nvec + splits - 1) / splits : nvec;
   const float s = FQ ? *fq_scale : 1.0f;
   float amax = 0.0f;
   bool mismatch = false;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+  const int n_items = SPLIT ? T * splits : T;
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < n_items; item += nw) {
+    const int t = SPLIT ? item / splits : item;
+    const int v_begin = SPLIT ? (item - t * splits) * per_part : 0;
+    const int v_end = SPLIT ? min(nvec, v_begin + per_part) : nvec;
     int my_p = -1;
     float my_w = 0.0f;
     if (lane < K) {
@@ -54,7 +64,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
       w[j] = __shfl_sync(0xffffffffu, my_w, j);
       if (j >= K) p[j] = -1;
     }
-    for (int v = lane; v < nvec; v += 32) {
+    for (int v = v_begin + lane; v < v_end; v += 32) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -121,16 +131,23 @@ moe_status_t launch_combine(const uint16_t* y, const int32_t* inv_map, const flo
                             const uint16_t* shared_y, const int32_t* shared_map, const float* fq_scale,
                             uint16_t* out, const uint16_t* expected, int32_t* dev_status, float* amax,
                             cudaStream_t s) {
-  const int blocks = min((T + 7) / 8, num_sms() * 16);
+  // split a token's columns over several warps when T warps cannot fill the GPU
+  const int target_warps = num_sms() * 16;
+  const int splits = std::max(1, std::min(H / 8 / 32, target_warps / std::max(T, 1)));
+  const long long items = (long long)T * splits;
+  const int blocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 16);
   const bool fq = fq_scale != nullptr && MODE != kAmax;
-#define MOE_COMBINE_LAUNCH(FQV, KM)                                                                    \
-  combine_kernel<MODE, FQV, KM><<<blocks, 256, 0, s>>>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, \
-                                                       fq_scale, out, expected, dev_status, amax)
-  if (K <= 8) {
-    if (fq) MOE_COMBINE_LAUNCH(true, 8); else MOE_COMBINE_LAUNCH(false, 8);
+#define MOE_COMBINE_LAUNCH(FQV, KM, SP)                                                                 \
+  combine_kernel<MODE, FQV, KM, SP><<<blocks, 256, 0, s>>>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, \
+                                                           fq_scale, out, expected, dev_status, amax, splits)
+#define MOE_COMBINE_LAUNCH_K(FQV, SP) \
+  if (K <= 8) MOE_COMBINE_LAUNCH(FQV, 8, SP); else MOE_COMBINE_LAUNCH(FQV, 32, SP);
+  if (splits > 1) {
+    if (fq) { MOE_COMBINE_LAUNCH_K(true, true) } else { MOE_COMBINE_LAUNCH_K(false, true) }
   } else {
-    if (fq) MOE_COMBINE_LAUNCH(true, 32); else MOE_COMBINE_LAUNCH(false, 32);
+    if (fq) { MOE_COMBINE_LAUNCH_K(true, false) } else { MOE_COMBINE_LAUNCH_K(false, false) }
   }
+#undef MOE_COMBINE_LAUNCH_K
 #undef MOE_COMBINE_LAUNCH
   MOE_CHECK_LAUNCH();
   return MOE_OK;

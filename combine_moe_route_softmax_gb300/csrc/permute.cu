@@ -276,28 +276,34 @@ __device__ __forceinline__ uint4 qdq8(const uint4 u, float s) {
 // Source-ordered gather: one warp per token, the row read once in chunks of 4 16-byte
 // vectors per lane and written to each destination row.  With a dispatch scale (DQ), the
 // routed destinations get the fake-quantised row and the shared row the original.
+// With few tokens (decode) a token's columns are split over `splits` warps, each taking
+// a run of whole 128-vector groups, so that the GPU has enough warps in flight.
 template <bool DQ>
 __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t* __restrict__ x, int T, int K,
                                                                   int H, const int32_t* __restrict__ inv_map,
                                                                   const int32_t* __restrict__ shared_map,
                                                                   const float* __restrict__ dq_scale,
-                                                                  uint16_t* __restrict__ xp) {
+                                                                  uint16_t* __restrict__ xp, int splits) {
   const int lane = threadIdx.x & 31;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / 8;
+  const int per_part = ((nvec + 127) / 128 + splits - 1) / splits * 128;   // vectors, whole groups
   const int ndst = K + 1;
   const float s = DQ ? *dq_scale : 1.0f;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * splits; item += nw) {
+    const int t = item / splits;
+    const int v_begin = (item - t * splits) * per_part;
+    const int v_end = min(nvec, v_begin + per_part);
     const int my_dst = token_dest(inv_map, shared_map, t, K, lane);
     const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
     if (!live) continue;                      // padding token: nothing to copy
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    for (int v0 = 0; v0 < nvec; v0 += 128) {
+    for (int v0 = v_begin; v0 < v_end; v0 += 128) {
       uint4 r[4], q[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int v = v0 + lane + 32 * j;
-        if (v < nvec) {
+        if (v < v_end) {
           r[j] = __ldg(in + v);
           if (DQ) q[j] = qdq8(r[j], s);
         }
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int v = v0 + lane + 32 * j;
-          if (v < nvec) o[v] = (DQ && routed) ? q[j] : r[j];
+          if (v < v_end) o[v] = (DQ && routed) ? q[j] : r[j];
         }
       }
     }
@@ -352,20 +358,25 @@ __global__ void __launch_bounds__(256) permute_gather_e4m3_kernel(const uint16_t
                                                                   int H, const int32_t* __restrict__ inv_map,
                                                                   const int32_t* __restrict__ shared_map,
                                                                   uint8_t* __restrict__ xp,
-                                                                  float* __restrict__ xp_scales) {
+                                                                  float* __restrict__ xp_scales, int splits) {
   const int lane = threadIdx.x & 31;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / 8;
   const int nblk = H / 128;
+  // parts of whole 32-vector groups (two 1x128 blocks), so each half-warp keeps one block
+  const int per_part = ((nvec + 31) / 32 + splits - 1) / splits * 32;
   const int ndst = K + 1;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * splits; item += nw) {
+    const int t = item / splits;
+    const int v_begin = (item - t * splits) * per_part;
+    const int v_end = min(nvec, v_begin + per_part);
     const int my_dst = token_dest(inv_map, shared_map, t, K, lane);
     const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
     if (!live) continue;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    for (int v0 = 0; v0 < nvec; v0 += 32) {
+    for (int v0 = v_begin; v0 < v_end; v0 += 32) {
       const int v = v0 + lane;
-      const bool ok = v < nvec;
+      const bool ok = v < v_end;
       const uint4 u = ok ? __ldg(in + v) : make_uint4(0, 0, 0, 0);
       float s;
       const uint2 q = quant8(u, ok, &s);
@@ -495,18 +506,22 @@ static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, i
                                                                   topk_w, row_w, batched ? max_tokens : 0,
                                                                   masked_m, dev_status);
   MOE_CHECK_LAUNCH();
-  const int gblocks = min((T + 7) / 8, num_sms() * 8);
+  // column parts per token: enough warps to fill the GPU when tokens are few
+  const int groups = out_dtype == MOE_BF16 ? (H / 8 + 127) / 128 : (H / 8 + 31) / 32;
+  const int splits = std::max(1, std::min(groups, num_sms() * 16 / T));
+  const long long items = (long long)T * splits;
+  const int gblocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 8);
   const int32_t* smap = with_shared ? shared_map : nullptr;
   if (out_dtype == MOE_BF16)
     if (dq_scale)
       permute_gather_bf16_kernel<true><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
-                                                               static_cast<uint16_t*>(xp));
+                                                               static_cast<uint16_t*>(xp), splits);
     else
       permute_gather_bf16_kernel<false><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, nullptr,
-                                                                static_cast<uint16_t*>(xp));
+                                                                static_cast<uint16_t*>(xp), splits);
   else
     permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint8_t*>(xp),
-                                                       xp_scales);
+                                                       xp_scales, splits);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

@@ -118,6 +118,20 @@ def test_permute_ragged_and_edge_shapes(T, K, E, pad, shared):
     check_permute(idx, E, x, shared, moe.MOE_E4M3)
 
 
+@pytest.mark.parametrize("T,H", [(1, 7168), (3, 7168), (130, 7168), (9, 1152), (200, 2048)])
+def test_permute_few_tokens_split_columns(T, H):
+    """Few tokens: each token's columns are gathered by several warps (parts of whole
+    vector groups; H = 1152 leaves a partial last group)."""
+    need_gpu()
+    rng = np.random.default_rng(T + H)
+    E, K = 40, 6
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    idx[rng.random((T, K)) < 0.1] = -1
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(H)).to(torch.bfloat16).cuda()
+    check_permute(idx, E, x, True, moe.MOE_BF16)
+    check_permute(idx, E, x, True, moe.MOE_E4M3)
+
+
 def test_permute_all_padding_and_bad_ids():
     need_gpu()
     x = torch.randn(64, 256).to(torch.bfloat16).cuda()
@@ -182,7 +196,10 @@ def combine_problem(T, K, E, H, pad, shared, seed, device="cuda"):
 
 @pytest.mark.parametrize("T,K,E,H,pad,shared,fq", [(333, 8, 64, 1024, 0.1, True, None), (333, 8, 64, 1024, 0.1, True, 37.5),
                                                    (50, 2, 8, 256, 0.0, False, None), (64, 12, 16, 384, 0.2, True, 3.0),
-                                                   (16384, 8, 256, 7168, 0.0, True, None)])
+                                                   (16384, 8, 256, 7168, 0.0, True, None),
+                                                   # few tokens: each row split over several warps (uneven parts)
+                                                   (1, 8, 64, 7168, 0.0, True, 12.0), (5, 8, 64, 7168, 0.1, True, None),
+                                                   (130, 8, 256, 7168, 0.0, True, None), (7, 4, 9, 1152, 0.2, False, 3.0)])
 def test_combine_bit_exact(T, K, E, H, pad, shared, fq):
     need_gpu()
     idx, inv, smap, y, wt = combine_problem(T, K, E, H, pad, shared, seed=T + K)

@@ -4,7 +4,7 @@ over one batch of the prefill workload (T = 8192 tokens in a 16384-row bucket,
 H = 7168, I = 2048, E = 256, top-8, one shared expert, BF16, Zipf(1.1) router skew).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
-                    [--layout contiguous|batched [--max-tokens M]]
+                    [--layout contiguous|batched [--max-tokens M]] [--fuse-combine]
 
 Prints one JSON line (rank 0).  `value` is layer tokens/s with inputs resident in HBM;
 `e2e` is the same metric through moe_layer_forward with the step's inputs copied from
@@ -135,7 +135,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device, max_tokens=0):
+def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -152,7 +152,7 @@ def workload_state(w, seed, device, max_tokens=0):
             kw.update(shared_w13=qs13, shared_w2=qs2, shared_w13_scales=cs13, shared_w2_scales=cs2)
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
-    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, **kw)
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine, **kw)
     st = dict(layer=layer, logits=logits, x=x,
               idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
               wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
@@ -208,6 +208,15 @@ def staged_step(st, w, events):
                                   d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                   p(st["status"]), s) == 0
     events[3].record()
+    if d.fuse_combine:
+        # down projection + combine in one launch: the combine stage below is empty
+        assert L.moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m if mt else v.cu_seqlens, nseg, mt, v.cap,
+                                          d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), d.dtype, v.y, None,
+                                          v.src_row, v.inv_map, p(st["wt"]), d.T, d.K, v.shared_map, None,
+                                          p(st["out"]), v.counters, p(st["status"]), s) == 0
+        events[4].record()
+        events[5].record()
+        return
     if mt:
         assert L.moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, nseg, mt, d.I, d.H, p(tw[1]), p(tw[5]),
                                           d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None,
@@ -259,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
     dist_init(world, "nccl")
     w = synth.WORKLOADS[args.workload]
     max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
-    st = workload_state(w, rank_seed(0, rank), device, max_tokens)
+    st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine)
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -408,8 +417,9 @@ def run_ours(args, rank, world, local_rank):
                    "tokens_per_step": w.T_valid, "parallelism": f"token-sharded replicas x{world}",
                    "layout": (f"batched [{w.E + int(w.shared)}, {max_tokens}, H] + masked_m" if max_tokens
                               else "contiguous expert-major rows + cu_seqlens"),
+                   "combine": "fused into the down projection" if args.fuse_combine else "separate kernel",
                    "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
-        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "gpu_launches": (sum(KERNELS_PER_STEP.values()) - int(args.fuse_combine)) * args.steps,
         "kernels": kernels,
         "rows": work["_rows"],
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
@@ -502,6 +512,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["contiguous", "batched"], default="contiguous",
                     help="expert-major rows with cu_seqlens, or the batched [E, max_tokens, H] layout")
+    ap.add_argument("--fuse-combine", action="store_true",
+                    help="run the combine inside the down projection (moe_grouped_gemm_combine)")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="rows per expert block of the batched layout (default: the bucket's T, which never "
                          "overflows)")

@@ -29,7 +29,7 @@ class MoeError(RuntimeError):
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
-                ("weight_in_down", _I), ("max_tokens", _I)]
+                ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -40,7 +40,7 @@ class LayerWeights(ctypes.Structure):
 class LayerViews(ctypes.Structure):
     _fields_ = [("xp", _P), ("xp_scales", _P), ("hs", _P), ("hs_scales", _P), ("y", _P), ("cu_seqlens", _P),
                 ("src_row", _P), ("inv_map", _P), ("shared_map", _P), ("row_weights", _P), ("cap", _I),
-                ("masked_m", _P)]
+                ("masked_m", _P), ("counters", _P)]
 
 
 # C signatures (restype int = moe_status_t unless noted)
@@ -63,6 +63,8 @@ _SIGS = {
     "moe_grouped_gemm_ex": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_batched": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P],
                                  _I),
+    "moe_grouped_gemm_combine": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I,
+                                  _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_combine_verify": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_combine_amax": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -274,6 +276,33 @@ def moe_grouped_gemm_batched(a, masked_m, w, a_scales=None, w_scales=None, w_ext
     return out, out_scales
 
 
+def moe_grouped_gemm_combine(a, seg, w, src_row, inv_map, topk_w, max_tokens=0, shared_map=None, fq_scale=None,
+                             a_scales=None, w_scales=None, w_extra=None, w_extra_scales=None, row_scale=None, y=None,
+                             out=None, counters=None, dev_status=None, stream=None):
+    """Down projection with the combine fused: a [rows, k] (or [S, max_tokens, k] with seg =
+    masked_m and max_tokens > 0; else seg = cu_seqlens), w [num_w, H, k]; returns (out [T, H],
+    y [rows, H], counters)."""
+    _dev(a)
+    fp8 = a.dtype == torch.uint8
+    k_dim = a.shape[-1]
+    rows = a.numel() // k_dim
+    num_w, H = w.shape[0], w.shape[1]
+    T, K = inv_map.shape
+    nseg = seg.numel() if max_tokens else seg.numel() - 1
+    if y is None:
+        y = torch.empty(rows, H, dtype=torch.bfloat16, device=a.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=a.device)
+    if counters is None:
+        counters = torch.zeros(T, H // 128, dtype=torch.int32, device=a.device)
+    _check("moe_grouped_gemm_combine", lib().moe_grouped_gemm_combine(
+        _ptr(a), _ptr(a_scales), _ptr(seg), nseg, max_tokens, rows, k_dim, H, _ptr(w), _ptr(w_scales), num_w,
+        _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, _ptr(y), _ptr(row_scale), _ptr(src_row),
+        _ptr(inv_map), _ptr(topk_w), T, K, _ptr(shared_map), _ptr(fq_scale), _ptr(out), _ptr(counters),
+        _ptr(dev_status), _stream(stream)))
+    return out, y, counters
+
+
 def moe_combine(y, inv_map, topk_w, shared_y=None, shared_map=None, fq_scale=None, out=None, stream=None):
     _dev(y)
     T, K = inv_map.shape
@@ -321,9 +350,9 @@ class MoeLayer:
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
-                 weight_in_down=False, max_tokens=0):
+                 weight_in_down=False, max_tokens=0, fuse_combine=False):
         self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
-                              int(max_tokens))
+                              int(max_tokens), int(fuse_combine))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

@@ -57,4 +57,13 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// The permute behind moe_permute / moe_permute_ex / moe_permute_batched (permute.cu);
+// zero_buf (nullable, [T, zero_per_token] int32) is cleared by its first kernel, for the
+// layer's fused combine counters.
+moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with_shared, const uint16_t* x, int H,
+                          moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens, int32_t* src_row,
+                          int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
+                          const float* dq_scale, const float* topk_w, float* row_w, int max_tokens,
+                          int32_t* masked_m, void* stream, int32_t* zero_buf, int zero_per_token);
+
 }  // namespace moe

@@ -85,6 +85,16 @@ struct Args {
   float* out_scales;
   int32_t* dev_status;
   const float* row_scale;   // plain epilogue: out row r is multiplied by row_scale[r] (nullable)
+  // fused combine (FUSE): out holds the BF16 expert rows; each token's output row is their
+  // fixed-order sum, computed by the warp whose store completes the token's 128-column block
+  const int32_t* src_row;   // row -> source index (t*K + k, or T*K + t for a shared row)
+  const int32_t* inv_map;   // [T, K] slot -> row or -1
+  const float* topk_w;      // [T, K] router weights, NULL for rows stored weighted
+  const int32_t* shared_map;  // [T] token -> shared row or -1 (nullable)
+  const float* fq_scale;    // combine fake-quant scale (nullable)
+  uint16_t* comb_out;       // [T, n_dim] BF16
+  int32_t* counters;        // [T, n_dim / 128], zero on entry, left zero
+  int T, K;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -257,8 +267,80 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, c
   return w;
 }
 
+// ----------------------------------------------------------------- fused combine
+// Columns [col, col + 128) of token t's output: the combine's arithmetic on the stored BF16
+// rows -- slots in ascending order, r = float(y) * w (float32 product), optional E4M3 QDQ,
+// float32 sum from +0 without FMA, the shared row last (only for a token with a routed
+// row), one BF16 rounding.  The whole warp works on the block: lane l owns 4 columns.  Rows
+// are read through L2 (__ldcg): other SMs wrote them.
+__device__ __forceinline__ void combine_block(const Args& args, int t, int col, int lane) {
+  const int K = args.K, H = args.n_dim;
+  const uint16_t* y = static_cast<const uint16_t*>(args.out);
+  const int c = col + 4 * lane;
+  const bool fq = args.fq_scale != nullptr;
+  const float s = fq ? *args.fq_scale : 1.0f;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  bool any = false;
+  constexpr int KB = 4;   // slots whose rows are loaded together
+  for (int k0 = 0; k0 < K; k0 += KB) {
+    int p[KB];
+    float wt[KB];
+    uint2 v[KB];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      const int k = k0 + j;
+      p[j] = k < K ? args.inv_map[(size_t)t * K + k] : -1;
+      wt[j] = (k < K && args.topk_w) ? args.topk_w[(size_t)t * K + k] : 1.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < KB; ++j)
+      if (p[j] >= 0) v[j] = __ldcg(reinterpret_cast<const uint2*>(y + (size_t)p[j] * H + c));
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      if (p[j] < 0) continue;
+      any = true;
+      const uint32_t u[2] = {v[j].x, v[j].y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float yv = __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16));
+        float r = __fmul_rn(yv, wt[j]);
+        if (fq) r = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(r, s))), s);
+        acc[i] = __fadd_rn(acc[i], r);
+      }
+    }
+  }
+  if (any && args.shared_map) {
+    const int sp = args.shared_map[t];
+    if (sp >= 0) {
+      const uint2 sv = __ldcg(reinterpret_cast<const uint2*>(y + (size_t)sp * H + c));
+      const uint32_t u[2] = {sv.x, sv.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        acc[i] = __fadd_rn(acc[i], __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16)));
+    }
+  }
+  uint2 o;
+  o.x = (uint32_t)f32_to_bf16(acc[0]) | ((uint32_t)f32_to_bf16(acc[1]) << 16);
+  o.y = (uint32_t)f32_to_bf16(acc[2]) | ((uint32_t)f32_to_bf16(acc[3]) << 16);
+  *reinterpret_cast<uint2*>(args.comb_out + (size_t)t * H + c) = o;
+}
+
+// Tokens with no row anywhere (no valid slot and no shared row) get +0, the combine's value
+// for them; warps [w0, w0 + nw) of the grid share the tokens.
+__device__ __forceinline__ void zero_rowless_tokens(const Args& args, int w0, int nw, int lane) {
+  const int nv = args.n_dim / 8;
+  for (int t = w0; t < args.T; t += nw) {
+    bool any = false;
+    for (int k = lane; k < args.K; k += 32) any |= args.inv_map[(size_t)t * args.K + k] >= 0;
+    const bool has_row = __any_sync(0xffffffffu, any) || (args.shared_map && args.shared_map[t] >= 0);
+    if (has_row) continue;
+    uint4* o = reinterpret_cast<uint4*>(args.comb_out + (size_t)t * args.n_dim);
+    for (int v = lane; v < nv; v += 32) o[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // ------------------------------------------------------------------------ kernel
-template <bool FP8, bool SWIGLU, bool PAIR>
+template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmBx, const __grid_constant__ CUtensorMap tmAh,
@@ -329,6 +411,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   const int n_tiles = SWIGLU ? (args.n_dim / 2) / 128 : (args.n_dim + BN - 1) / BN;
   const int total_units = prefix[nseg] * n_tiles;
+  if (FUSE && total_units == 0) {
+    // no rows at all: every token's output is +0
+    zero_rowless_tokens(args, blockIdx.x * (THREADS / 32) + warp, gridDim.x * (THREADS / 32), lane);
+    return;
+  }
   if (static_cast<int>(blockIdx.x) >= total_units) return;  // no work: nothing allocated yet
 
   if (warp == 1) {
@@ -458,6 +545,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     int buf = 0;
     uint32_t tphase = 0;
     const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
+    if (FUSE) {
+      // while the first accumulator fills: +0 rows for the tokens no unit will touch
+      const int active = min((int)gridDim.x, total_units);
+      zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
+    }
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
       const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
       const int row = w.row0 + r_in_tile;
@@ -616,6 +708,45 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           __syncwarp();
         }
+        if (FUSE) {
+          // Rows [row0 + 32q, + rows_here) x columns [col0, col0 + 128) are stored.  Each lane
+          // counts its row in the (token, 128-column block) counter; the lane whose count
+          // completes the token's rows (its valid slots + its shared row) has its warp sum
+          // the block.  Every lane's stores are fenced before the counts (release); the
+          // summing warp fences again before it reads the rows (acquire).  No CTA waits.
+          __threadfence();
+          __syncwarp();
+          int done_t = -1;
+          if (lane < rows_here) {
+            const int src = args.src_row[w.row0 + 32 * q + lane];
+            const int TK = args.T * args.K;
+            const int t = src < TK ? src / args.K : src - TK;
+            if (src >= 0 && t < args.T) {
+              // rows of token t: its valid slots and its shared row (loads issued together)
+              int target = 0;
+              for (int k0 = 0; k0 < args.K; k0 += 8) {
+                int pv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) pv[j] = k0 + j < args.K ? args.inv_map[(size_t)t * args.K + k0 + j] : -1;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) target += pv[j] >= 0;
+              }
+              if (args.shared_map && args.shared_map[t] >= 0) ++target;
+              int32_t* cnt = args.counters + (size_t)t * (args.n_dim / 128) + col0 / 128;
+              if (atomicAdd(cnt, 1) == target - 1) {
+                *cnt = 0;   // every row of this block has arrived: reset for the next call
+                done_t = t;
+              }
+            }
+          }
+          unsigned m = __ballot_sync(0xffffffffu, done_t >= 0);
+          if (m) __threadfence();
+          while (m) {
+            const int l = __ffs(m) - 1;
+            m &= m - 1;
+            combine_block(args, __shfl_sync(0xffffffffu, done_t, l), col0, lane);
+          }
+        }
       }
     }
   }
@@ -655,10 +786,10 @@ bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, bool SWIGLU, bool PAIR>
+template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
 moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
                         const Args& args, int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR>;
+  auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR, FUSE>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
@@ -684,11 +815,11 @@ moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 
 // CTA pairs (2-CTA clusters sharing A) when the unit count per m-tile is even, so the two
 // CTAs of a pair always hold two n-tiles of one m-tile.
-template <bool FP8, bool SWIGLU>
+template <bool FP8, bool SWIGLU, bool FUSE = false>
 moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
                     const Args& args, int grid, bool pair, cudaStream_t s) {
-  if (pair) return launch_one<FP8, SWIGLU, true>(a, b, bx, ah, args, grid & ~1, s);
-  return launch_one<FP8, SWIGLU, false>(a, b, bx, ah, args, grid, s);
+  if (pair) return launch_one<FP8, SWIGLU, true, FUSE>(a, b, bx, ah, args, grid & ~1, s);
+  return launch_one<FP8, SWIGLU, false, FUSE>(a, b, bx, ah, args, grid, s);
 }
 
 }  // namespace gg
@@ -696,13 +827,26 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMa
 
 namespace moe {
 namespace gg {
+struct FuseIn {
+  const int32_t* src_row;
+  const int32_t* inv_map;
+  const float* topk_w;
+  const int32_t* shared_map;
+  const float* fq_scale;
+  uint16_t* out;
+  int32_t* counters;
+  int T, K;
+};
+
 // max_tokens == 0: segments from cu_seqlens over rows_cap rows; > 0: batched segments
-// (bounds = masked_m) over rows_cap = num_segments * max_tokens rows.
+// (bounds = masked_m) over rows_cap = num_segments * max_tokens rows.  fuse: the down
+// projection with the combine fused into its epilogue.
 static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_t* cu_seqlens, int max_tokens,
                               int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,
                               const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
                               moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
-                              int32_t* dev_status, const float* row_scale, void* stream) {
+                              int32_t* dev_status, const float* row_scale, void* stream,
+                              const FuseIn* fuse = nullptr) {
   const bool fp8 = dtype == MOE_E4M3;
   const bool swiglu = epilogue == MOE_EPI_SWIGLU;
   if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -712,6 +856,15 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   if (k_dim <= 0 || k_dim % 128 != 0 || n_dim <= 0 || n_dim % 128 != 0) return MOE_ERR_ARG;
   if (swiglu && (n_dim % 256 != 0)) return MOE_ERR_ARG;
   if (swiglu && row_scale) return MOE_ERR_ARG;
+  if (fuse) {
+    if (swiglu || fuse->T < 0 || fuse->K < 1 || fuse->K > kMaxTopK) return MOE_ERR_ARG;
+    if (fuse->T == 0) return MOE_OK;
+    if (!fuse->src_row || !fuse->inv_map || !fuse->out || !fuse->counters) return MOE_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(fuse->out) & 15) return MOE_ERR_ARG;
+    // every token's output is written by this call, so it needs at least one row of capacity
+    if (num_segments == 0 || rows_cap == 0) return MOE_ERR_ARG;
+    if ((long long)fuse->T * fuse->K + fuse->T > 0x7fffffffll) return MOE_ERR_ARG;
+  }
   if (num_segments == 0 || rows_cap == 0) return MOE_OK;
   if (!a || !cu_seqlens || !out || (num_w > 0 && !w)) return MOE_ERR_ARG;
   if (fp8 && (!a_scales || (num_w > 0 && !w_scales) || (w_extra && !w_extra_scales))) return MOE_ERR_ARG;
@@ -746,12 +899,24 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   args.out_scales = out_scales;
   args.dev_status = dev_status;
   args.row_scale = row_scale;
+  args.src_row = fuse ? fuse->src_row : nullptr;
+  args.inv_map = fuse ? fuse->inv_map : nullptr;
+  args.topk_w = fuse ? fuse->topk_w : nullptr;
+  args.shared_map = fuse ? fuse->shared_map : nullptr;
+  args.fq_scale = fuse ? fuse->fq_scale : nullptr;
+  args.comb_out = fuse ? fuse->out : nullptr;
+  args.counters = fuse ? fuse->counters : nullptr;
+  args.T = fuse ? fuse->T : 0;
+  args.K = fuse ? fuse->K : 1;
   // grid: one CTA per SM, never more than the largest possible number of tiles
   const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
   const int grid = (int)std::min<long long>(num_sms(), max_units);
   const bool pair = n_tiles % 2 == 0 && grid >= 2;
   cudaStream_t s = as_stream(stream);
+  if (fuse)
+    return fp8 ? launch<true, false, true>(ma, mb, mbx, mah, args, grid, pair, s)
+               : launch<false, false, true>(ma, mb, mbx, mah, args, grid, pair, s);
   if (fp8)
     return swiglu ? launch<true, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<true, false>(ma, mb, mbx, mah, args, grid, pair, s);
   return swiglu ? launch<false, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<false, false>(ma, mb, mbx, mah, args, grid, pair, s);
@@ -767,6 +932,23 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
                                             const float* row_scale, void* stream) {
   return moe::gg::gemm_impl(a, a_scales, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
                             w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_combine(
+    const void* a, const float* a_scales, const int32_t* seg, int num_segments, int max_tokens, int rows_cap,
+    int k_dim, int n_dim, const void* w, const float* w_scales, int num_w, const void* w_extra,
+    const float* w_extra_scales, moe_dtype_t dtype, uint16_t* y, const float* row_scale, const int32_t* src_row,
+    const int32_t* inv_map, const float* topk_w, int T, int K, const int32_t* shared_map, const float* fq_scale,
+    uint16_t* out, int32_t* counters, int32_t* dev_status, void* stream) {
+  if (max_tokens < 0) return MOE_ERR_ARG;
+  if (max_tokens > 0) {
+    if (num_segments < 0 || (long long)num_segments * max_tokens > 0x7fffffffll) return MOE_ERR_ARG;
+    rows_cap = num_segments * max_tokens;
+  }
+  const moe::gg::FuseIn f{src_row, inv_map, topk_w, shared_map, fq_scale, out, counters, T, K};
+  return moe::gg::gemm_impl(a, a_scales, seg, max_tokens, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
+                            w_extra, w_extra_scales, dtype, MOE_EPI_NONE, y, nullptr, dev_status, row_scale, stream,
+                            &f);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_batched(const void* a, const float* a_scales, const int32_t* masked_m,

@@ -16,7 +16,8 @@
 namespace moe {
 
 struct LayerPlan {
-  size_t off_cu, off_src, off_inv, off_smap, off_roww, off_scratch, off_xp, off_xps, off_hs, off_hss, off_y, total;
+  size_t off_cu, off_src, off_inv, off_smap, off_roww, off_scratch, off_xp, off_xps, off_hs, off_hss, off_y, off_cnt,
+      total;
   size_t scratch_bytes;
   int cap, nseg;
 };
@@ -28,6 +29,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
   if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E < 1 || d->E > kMaxExperts || d->K < 1 || d->K > d->E ||
       d->K > kMaxTopK || d->H % 128 || d->I % 128 || (d->has_shared != 0 && d->has_shared != 1) ||
       (d->weight_in_down != 0 && d->weight_in_down != 1) || d->max_tokens < 0 ||
+      (d->fuse_combine != 0 && d->fuse_combine != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -53,6 +55,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
   p->off_hs = o;      o = align256(o + cap * I * esz);
   p->off_hss = o;     o = align256(o + (fp8 ? cap * (I / 128) * 4 : 0));
   p->off_y = o;       o = align256(o + cap * H * 2);
+  p->off_cnt = o;     o = align256(o + (d->fuse_combine ? T * (H / 128) * 4 : 0));
   p->total = o;
   return true;
 }
@@ -82,6 +85,7 @@ extern "C" moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe
   v->hs = b + p.off_hs;
   v->hs_scales = fp8 ? reinterpret_cast<float*>(b + p.off_hss) : nullptr;
   v->y = reinterpret_cast<uint16_t*>(b + p.off_y);
+  v->counters = d->fuse_combine ? reinterpret_cast<int32_t*>(b + p.off_cnt) : nullptr;
   v->cap = p.cap;
   return MOE_OK;
 }
@@ -119,15 +123,21 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   if (d->max_tokens > 0) {
     // batched layout: same steps, segment s in rows [s*max_tokens, s*max_tokens + masked_m[s])
     const int mt = d->max_tokens;
-    st = moe_permute_batched(topk_idx, d->T, d->K, d->E, d->has_shared, mt, x, d->H, d->dtype, v.xp, v.xp_scales,
-                             v.masked_m, v.src_row, v.inv_map, v.shared_map,
-                             static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes, dev_status,
-                             dispatch_scale, wd ? topk_w : nullptr, wd ? v.row_weights : nullptr, stream);
+    if (mt < 1) return MOE_ERR_ARG;
+    st = permute_impl(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, nullptr,
+                      v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch,
+                      p.scratch_bytes, dev_status, dispatch_scale, wd ? topk_w : nullptr,
+                      wd ? v.row_weights : nullptr, mt, v.masked_m, stream, v.counters, d->H / 128);
     if (st != MOE_OK) return st;
     st = moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, p.nseg, mt, d->H, 2 * d->I, w->w13,
                                   w->w13_scales, d->E, sx13, sx13s, d->dtype, MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                   dev_status, nullptr, stream);
     if (st != MOE_OK) return st;
+    if (d->fuse_combine)
+      return moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m, p.nseg, mt, 0, d->I, d->H, w->w2,
+                                      w->w2_scales, d->E, sx2, sx2s, d->dtype, v.y, wd ? v.row_weights : nullptr,
+                                      v.src_row, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, v.shared_map,
+                                      fq_scale, out, v.counters, dev_status, stream);
     st = moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, p.nseg, mt, d->I, d->H, w->w2, w->w2_scales,
                                   d->E, sx2, sx2s, d->dtype, MOE_EPI_NONE, v.y, nullptr, dev_status,
                                   wd ? v.row_weights : nullptr, stream);
@@ -135,15 +145,20 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
     return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
                        v.shared_map, fq_scale, out, stream);
   }
-  st = moe_permute_ex(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales,
-                      v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch,
-                      p.scratch_bytes, dev_status, dispatch_scale, wd ? topk_w : nullptr,
-                      wd ? v.row_weights : nullptr, stream);
+  st = permute_impl(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, v.cu_seqlens,
+                    v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes,
+                    dev_status, dispatch_scale, wd ? topk_w : nullptr, wd ? v.row_weights : nullptr, 0, nullptr,
+                    stream, v.counters, d->H / 128);
   if (st != MOE_OK) return st;
   st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
                         sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
                         v.hs_scales, dev_status, stream);
   if (st != MOE_OK) return st;
+  if (d->fuse_combine)
+    return moe_grouped_gemm_combine(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, 0, p.cap, d->I, d->H, w->w2,
+                                    w->w2_scales, d->E, sx2, sx2s, d->dtype, v.y, wd ? v.row_weights : nullptr,
+                                    v.src_row, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, v.shared_map, fq_scale,
+                                    out, v.counters, dev_status, stream);
   st = moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, w->w2_scales, d->E,
                            sx2, d->has_shared ? w->shared_w2_scales : nullptr, d->dtype, MOE_EPI_NONE, v.y, nullptr,
                            dev_status, wd ? v.row_weights : nullptr, stream);

@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32
                                                                      int K, int E, int with_shared,
                                                                      int32_t* __restrict__ counts,
                                                                      int32_t* __restrict__ ticket,
-                                                                     int32_t* dev_status) {
+                                                                     int32_t* dev_status,
+                                                                     int32_t* __restrict__ zero_buf,
+                                                                     int zero_per_token) {
   extern __shared__ int hist[];
   const int nseg = E + with_shared;
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) hist[i] = 0;
@@ -60,6 +62,11 @@ __global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32
   }
   if (bad && dev_status) atomicOr(dev_status, MOE_DEV_BAD_EXPERT);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
+  if (zero_buf) {
+    // per-token counters of a later fused combine, cleared for this block's tokens
+    for (int i = threadIdx.x; i < (t1 - t0) * zero_per_token; i += blockDim.x)
+      zero_buf[(size_t)t0 * zero_per_token + i] = 0;
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) counts[(size_t)i * gridDim.x + blockIdx.x] = hist[i];
 }
@@ -449,11 +456,12 @@ extern "C" size_t moe_permute_batched_workspace_bytes(int T, int K, int E, int w
 }
 
 namespace moe {
-static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with_shared, const uint16_t* x,
-                                 int H, moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens,
-                                 int32_t* src_row, int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
-                                 int32_t* dev_status, const float* dq_scale, const float* topk_w, float* row_w,
-                                 int max_tokens, int32_t* masked_m, void* stream) {
+moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with_shared, const uint16_t* x,
+                          int H, moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens,
+                          int32_t* src_row, int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
+                          int32_t* dev_status, const float* dq_scale, const float* topk_w, float* row_w,
+                          int max_tokens, int32_t* masked_m, void* stream, int32_t* zero_buf,
+                          int zero_per_token){
   if (T < 0 || K < 1 || K > kMaxTopK || E < 1 || E > kMaxExperts || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
   if (with_shared != 0 && with_shared != 1) return MOE_ERR_ARG;
   if (out_dtype != MOE_BF16 && out_dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -491,7 +499,8 @@ static moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, i
   if (batched) cu_seqlens = reinterpret_cast<int32_t*>(base + lay.total);
   const int cap = batched ? nseg * max_tokens : T * K + (with_shared ? T : 0);
   permute_count_kernel<<<nblk, kPermThreads, nseg * sizeof(int), s>>>(topk_idx, T, K, E, with_shared, counts,
-                                                                        ticket, dev_status);
+                                                                        ticket, dev_status, zero_buf,
+                                                                        zero_per_token);
   MOE_CHECK_LAUNCH();
   permute_scan_kernel<<<nseg, 256, 0, s>>>(counts, nblk, nseg, seg_total, ticket, cu_seqlens);
   MOE_CHECK_LAUNCH();
@@ -534,7 +543,7 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E
                                     void* stream) {
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, nullptr, nullptr, nullptr, 0, nullptr,
-                           stream);
+                           stream, nullptr, 0);
 }
 
 extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, int E, int with_shared,
@@ -545,7 +554,7 @@ extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, in
                                        void* stream) {
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights, 0,
-                           nullptr, stream);
+                           nullptr, stream, nullptr, 0);
 }
 
 extern "C" moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int K, int E, int with_shared,
@@ -557,7 +566,7 @@ extern "C" moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int 
   if (max_tokens < 1) return MOE_ERR_ARG;
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xb, xb_scales, nullptr, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights,
-                           max_tokens, masked_m, stream);
+                           max_tokens, masked_m, stream, nullptr, 0);
 }
 
 extern "C" moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,

@@ -262,6 +262,37 @@ moe_status_t moe_grouped_gemm_batched(const void* a, const float* a_scales, cons
                                       void* out, float* out_scales, int32_t* dev_status,
                                       const float* row_scale, void* stream);
 
+/* ------------------------------------------------------- down projection + combine
+ * The down projection with the combine fused into its epilogue ([MegaMoE]: one kernel
+ * runs the expert GEMMs and the combine and leaves the weighted per-(token, slot) rows in
+ * its buffer; here only the single-GPU part of that idea: no dispatch, no all-to-all).
+ * It computes exactly what moe_grouped_gemm_ex (MOE_EPI_NONE) into y followed by
+ * moe_combine(y, inv_map, topk_w, T, K, n_dim, y, shared_map, fq_scale, out) computes, bit for
+ * bit, without the second launch and without reading y back from HBM: the warp whose
+ * stores complete a token's rows in a 128-column block sums that block from L2 in the
+ * combine's fixed order (a "last writer sums" scheme; the counts are atomic, the sums are
+ * not, and no block ever waits for another).
+ *   a ... dtype   as moe_grouped_gemm_ex; seg is cu_seqlens [num_segments + 1] when
+ *              max_tokens == 0 (rows_cap rows), or masked_m [num_segments] of the batched
+ *              layout when max_tokens > 0 (rows_cap is then num_segments * max_tokens).
+ *   y          out BF16 [rows_cap, n_dim]: the expert rows (router-weighted if row_scale).
+ *   src_row    int32 [rows_cap] from the permute (row -> t*K + k, or T*K + t for a shared row).
+ *   inv_map, topk_w (nullable: rows already weighted), T, K, shared_map (nullable),
+ *   fq_scale (nullable)   as moe_combine, with H = n_dim and y as the shared rows.
+ *   out        BF16 [T, n_dim], every row written (+0 for a token with no row).
+ *   counters   int32 [T, n_dim/128]: zero on entry; the call leaves it zero (after a
+ *              MOE_DEV_PIPELINE_TIMEOUT the caller zeroes it again).
+ * Errors: those of moe_grouped_gemm_ex; MOE_ERR_ARG for a null src_row / inv_map / out /
+ * counters, or T > 0 with no row capacity. */
+moe_status_t moe_grouped_gemm_combine(const void* a, const float* a_scales, const int32_t* seg,
+                                      int num_segments, int max_tokens, int rows_cap, int k_dim, int n_dim,
+                                      const void* w, const float* w_scales, int num_w, const void* w_extra,
+                                      const float* w_extra_scales, moe_dtype_t dtype, uint16_t* y,
+                                      const float* row_scale, const int32_t* src_row, const int32_t* inv_map,
+                                      const float* topk_w, int T, int K, const int32_t* shared_map,
+                                      const float* fq_scale, uint16_t* out, int32_t* counters,
+                                      int32_t* dev_status, void* stream);
+
 /* -------------------------------------------------------------------------- combine
  * Fixed-order combine ([MegaMoE]: each token's router-weighted slot rows are added in
  * increasing slot order into a float32 accumulator that starts at zero, rounded to BF16
@@ -323,6 +354,8 @@ typedef struct {
   int max_tokens;     /* 0: contiguous expert-major layout (cu_seqlens); > 0: the batched
                          layout, max_tokens rows per segment (the shared expert's included),
                          through moe_permute_batched / moe_grouped_gemm_batched (ABI 3) */
+  int fuse_combine;   /* 1: the combine runs inside the down projection
+                         (moe_grouped_gemm_combine); same output bit for bit (ABI 3) */
 } moe_layer_desc_t;
 
 typedef struct {
@@ -349,6 +382,7 @@ typedef struct {
   int cap;                      /* T*K + (has_shared ? T : 0); batched: nseg * max_tokens */
   int32_t* masked_m;            /* batched layout: [E + has_shared] rows per segment; else NULL
                                    (and cu_seqlens is NULL in the batched layout) */
+  int32_t* counters;            /* fuse_combine: [T, H/128] (zeroed by the layer's permute); else NULL */
 } moe_layer_views_t;
 
 /* Workspace bytes for a layer of this shape (0 for an invalid descriptor). */

@@ -65,6 +65,14 @@ def test_layer_workspace_size(lib):
     views = moe.LayerViews()
     assert lib.moe_layer_views(ctypes.byref(db), 1 << 20, ctypes.byref(views)) == 0
     assert views.cap == 257 * 128 and views.cu_seqlens is None and views.masked_m == 1 << 20
+    # fused combine: one more region, the [T, H/128] counters
+    df = moe.LayerDesc(128, 7168, 2048, 256, 8, moe.MOE_E4M3, 1, 0, 0, 1)
+    d0 = moe.LayerDesc(128, 7168, 2048, 256, 8, moe.MOE_E4M3, 1, 0, 0, 0)
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(df)) == lib.moe_layer_workspace_bytes(ctypes.byref(d0)) + \
+        128 * 56 * 4
+    assert lib.moe_layer_views(ctypes.byref(df), 1 << 20, ctypes.byref(views)) == 0 and views.counters
+    df.fuse_combine = 2
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(df)) == 0
     db.max_tokens = -1
     assert lib.moe_layer_workspace_bytes(ctypes.byref(db)) == 0
     db.max_tokens = 1 << 24   # 257 blocks of 2^24 rows: more than 2^31 rows
@@ -86,3 +94,8 @@ def test_argument_errors_launch_nothing(lib):
                                         None, None, None, None) == 1
     assert lib.moe_grouped_gemm_batched(None, None, None, 1025, 1 << 22, 128, 256, None, None, 1025, None, None, 0,
                                         0, None, None, None, None, None) == 1
+    # fused down projection + combine: tokens but no row capacity, or K out of range
+    assert lib.moe_grouped_gemm_combine(None, None, None, 0, 0, 0, 128, 256, None, None, 1, None, None, 0, None,
+                                        None, None, None, None, 4, 2, None, None, None, None, None, None) == 1
+    assert lib.moe_grouped_gemm_combine(None, None, None, 1, 0, 16, 128, 256, None, None, 1, None, None, 0, None,
+                                        None, None, None, None, 4, 33, None, None, None, None, None, None) == 1

@@ -23,6 +23,8 @@ lm_eval / OLMoE runs need datasets and trained weights, which these stand in for
   per-expert bias -1.1*ln(rank+1) over a seeded permutation rank (Zipf(1.1) popularity).
 * ``prefill_small`` the prefill shapes with E=32 and T=2048 tokens in a 4096-row bucket
   (about 4 GB on the device), for hardware-counter profiles.
+* ``decode_small`` the decode shapes with E=64 (2.8 GB of E4M3 weights), for
+  hardware-counter profiles of the FP8 kernels.
 * ``prefill_fq`` the prefill workload with the combine's constant-scale FP8
   fake-quant; the scale comes from a calibration batch drawn with seed + 1.
 
@@ -60,6 +62,8 @@ WORKLOADS = {
     # prefill shapes with fewer experts and tokens (about 4 GB on the device): the case
     # full hardware-counter profiles are taken on
     "prefill_small": Workload("prefill_small", 4096, 2048, 7168, 2048, 32, 8, True, "bf16", "zipf", 0.0),
+    # decode shapes with 64 experts (2.8 GB of E4M3 weights): the FP8 kernels' profiling case
+    "decode_small": Workload("decode_small", 128, 128, 7168, 2048, 64, 8, True, "e4m3", "uniform", 0.0),
     "prefill_fq": Workload("prefill_fq", 16384, 8192, 7168, 2048, 256, 8, True, "bf16", "zipf",
                            0.0, fake_quant=True, graph=True),
 }

@@ -131,8 +131,9 @@ moe_status_t launch_combine(const uint16_t* y, const int32_t* inv_map, const flo
                             const uint16_t* shared_y, const int32_t* shared_map, const float* fq_scale,
                             uint16_t* out, const uint16_t* expected, int32_t* dev_status, float* amax,
                             cudaStream_t s) {
-  // split a token's columns over several warps when T warps cannot fill the GPU
-  const int target_warps = num_sms() * 16;
+  // split a token's columns over several warps when T warps cannot fill the GPU (64
+  // resident warps per SM)
+  const int target_warps = num_sms() * 64;
   const int splits = std::max(1, std::min(H / 8 / 32, target_warps / std::max(T, 1)));
   const long long items = (long long)T * splits;
   const int blocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 16);

@@ -517,7 +517,7 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
   MOE_CHECK_LAUNCH();
   // column parts per token: enough warps to fill the GPU when tokens are few
   const int groups = out_dtype == MOE_BF16 ? (H / 8 + 127) / 128 : (H / 8 + 31) / 32;
-  const int splits = std::max(1, std::min(groups, num_sms() * 16 / T));
+  const int splits = std::max(1, std::min(groups, num_sms() * 64 / T));   // 64 resident warps per SM
   const long long items = (long long)T * splits;
   const int gblocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 8);
   const int32_t* smap = with_shared ? shared_map : nullptr;

@@ -183,7 +183,7 @@ def run_layer(w, max_tokens, seed=0, weight_in_down=False, fq=None):
     return out, st.item(), (logits, x, w13, w2, s13, s2, kw, idx, wt)
 
 
-@pytest.mark.parametrize("case", ["tiny", "decode_small", "prefill_small_wd", "decode_fp8"])
+@pytest.mark.parametrize("case", ["tiny", "decode_small", "prefill_small_wd", "decode_fp8", "decode_full"])
 def test_layer_batched_equals_contiguous(case):
     need_gpu()
     wd, fq = False, None
@@ -196,9 +196,12 @@ def test_layer_batched_equals_contiguous(case):
     elif case == "prefill_small_wd":
         w = scaled(WORKLOADS["prefill"], T=128, T_valid=100, H=512, I=256, E=16, K=4)
         mt, wd, fq = 128, True, 30.0
-    else:
+    elif case == "decode_fp8":
         w = scaled(WORKLOADS["decode"], T=128, T_valid=128, H=1024, I=512, E=64, K=8)
         mt = 128
+    else:
+        w = WORKLOADS["decode"]          # full size: 257 blocks of 128 rows
+        mt = w.T
     out_b, st_b, _ = run_layer(w, mt, weight_in_down=wd, fq=fq)
     out_c, st_c, _ = run_layer(w, 0, weight_in_down=wd, fq=fq)
     assert st_b == 0 and st_c == 0

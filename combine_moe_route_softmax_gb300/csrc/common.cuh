@@ -6,6 +6,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 #define MOE_CHECK_LAUNCH()                                   \
@@ -18,15 +20,31 @@ namespace moe {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 
+// SM count of the current device (cached per device; 1 -- always a valid grid size -- if
+// the query fails).
 inline int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::atomic<int>& c = cache[dev & 63];
+  int n = c.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  c.store(n, std::memory_order_relaxed);
   return n;
+}
+
+// Function attributes live in each device's context: run `set` (returning true on success)
+// once per device.  Concurrent first calls may both run it, which is harmless.
+template <class F>
+inline bool once_per_device(std::atomic<unsigned long long>& done, F&& set) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return true;
+  if (!set()) return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
 }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -790,12 +790,12 @@ template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
 moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
                         const Args& args, int grid, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR, FUSE>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
+               cudaSuccess;
+      }))
+    return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);

@@ -505,11 +505,8 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
   permute_scan_kernel<<<nseg, 256, 0, s>>>(counts, nblk, nseg, seg_total, ticket, cu_seqlens);
   MOE_CHECK_LAUNCH();
   const size_t scatter_smem = (size_t)kPermWarps * nseg * sizeof(int);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    attr_set = true;
-  }
+  // per-warp histograms of up to 1025 segments: 32.8 KB, under the 48 KB default limit
+  static_assert(kPermWarps * (kMaxExperts + 1) * sizeof(int) <= 48 * 1024, "scatter histograms exceed 48 KB");
   permute_scatter_kernel<<<nblk, kPermThreads, scatter_smem, s>>>(topk_idx, T, K, E, with_shared, counts,
                                                                   cu_seqlens, cap, src_row, inv_map, shared_map,
                                                                   topk_w, row_w, batched ? max_tokens : 0,

@@ -126,3 +126,31 @@ def test_fp8_layer_replayed_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert b["st"].item() == 0
     assert np.array_equal(bits(b["out"]), eager)
+
+
+def test_one_graph_replayed_at_every_bucket_fill():
+    """A layer captured once serves batches of any fill of its bucket: num_tokens is read on
+    the device, so each replay routes, permutes and combines only the first n rows (the
+    rest come out +0), bit-identical to an eager call with the same n."""
+    need_gpu()
+    w = scaled(WORKLOADS["prefill"], T=256, T_valid=256, H=512, I=256, E=16, K=4)
+    x, logits, _, layer, b = make_layer(w)
+    run = lambda: layer.forward(x, b["out"], b["idx"], b["wt"], logits=logits, num_tokens=b["n"],
+                                dev_status=b["st"])
+    run()                                       # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for n in (256, 0, 1, 37, 200, 256):
+        b["n"].fill_(n)
+        b["out"].fill_(7.0)
+        run()
+        torch.cuda.synchronize()
+        eager = bits(b["out"]).copy()
+        b["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert b["st"].item() == 0
+        assert np.array_equal(bits(b["out"]), eager), n
+        assert np.all(eager[n:] == 0) and np.all(host(b["idx"])[n:] == -1)

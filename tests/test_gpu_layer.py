@@ -110,6 +110,32 @@ def test_layer_prefill_full_size_sampled():
     assert np.array_equal(host(s.layer.view("src_row", (cap,), torch.int32)), src)
     assert np.array_equal(host(s.layer.view("inv_map", (16384, 8), torch.int32)), inv)
     assert v.cap == cap
+    # every token: the output is the fixed-order re-sum of the layer's own expert rows
+    H = 7168
+    y = s.layer.view("y", (cap, H), torch.bfloat16)
+    vs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_combine_verify(y, s.layer.view("inv_map", (16384, 8), torch.int32), s.topk_w, s.out, vs, shared_y=y,
+                           shared_map=s.layer.view("shared_map", (16384,), torch.int32))
+    torch.cuda.synchronize()
+    assert vs.item() == 0
+    # expert rows of 48 distinct experts (and the shared expert), each against the oracle's
+    # SwiGLU expert on its token: every grouped-GEMM segment kind, checked row by row
+    rng = np.random.default_rng(3)
+    n_routed = int(cu[256])
+    seg_of = np.searchsorted(cu, np.arange(int(cu[-1])), side="right") - 1
+    experts = rng.choice(np.unique(seg_of[:n_routed]), size=48, replace=False)
+    rows = [int(rng.choice(np.nonzero(seg_of == e)[0])) for e in experts]
+    rows.append(int(rng.integers(n_routed, int(cu[-1]))))              # a shared-expert row
+    xb = bits(s.x)
+    yb = bits(y)
+    for r in rows:
+        e = int(seg_of[r])
+        tok = int(ref.row_tokens(src[r:r + 1], 16384, 8)[0])
+        f = lambda t: bf16_bits_to_f32(t).astype(np.float64)
+        w13, w2 = (bits(s.s13), bits(s.s2)) if e == 256 else (bits(s.w13[e]), bits(s.w2[e]))
+        want = ref.swiglu_expert(f(xb[tok:tok + 1]), f(w13), f(w2))[0]
+        got = bf16_bits_to_f32(yb[r]).astype(np.float64)
+        assert ref.max_rel_err(got, want) <= TOL["bf16"], (r, e)
 
 
 def test_layer_decode_full_size_sampled():
@@ -117,6 +143,18 @@ def test_layer_decode_full_size_sampled():
     s = Setup(WORKLOADS["decode"])
     tokens = sample_tokens(128, 2, seed=2)[:2]
     err = check_layer(s, tokens, TOL["e4m3"])
+    # every token: the output is the fixed-order re-sum of the layer's own expert rows, and
+    # the layout is the oracle's
+    cap = 128 * 8 + 128
+    y = s.layer.view("y", (cap, 7168), torch.bfloat16)
+    inv = s.layer.view("inv_map", (128, 8), torch.int32)
+    smap = s.layer.view("shared_map", (128,), torch.int32)
+    vs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_combine_verify(y, inv, s.topk_w, s.out, vs, shared_y=y, shared_map=smap)
+    torch.cuda.synchronize()
+    assert vs.item() == 0
+    cu, src, o_inv, o_smap, _ = ref.permute(s.o_idx, 256, with_shared=True)
+    assert np.array_equal(host(inv), o_inv) and np.array_equal(host(smap), o_smap)
     # against the unquantised BF16 masters the difference is FP8's own rounding error
     got = bf16_bits_to_f32(bits(s.out)).astype(np.float64)[tokens]
     err_master = ref.max_rel_err(got, s.reference(tokens, fp8=False))

@@ -8,10 +8,25 @@
 // cancels, w_k = e^{l_k - l_max} / sum_j e^{l_j - l_max}.
 //
 // Bound: HBM, T*E*4 bytes read + T*K*8 written; one warp reads its token's E logits
-// with coalesced loads (lane l holds experts l, l+32, ...).
+// with coalesced loads (lane l holds experts l, l+32, ...).  Each of the K selection rounds
+// is one 64-bit max per lane and a 5-step warp butterfly on packed (logit, id) keys.
 #include "common.cuh"
 
 namespace moe {
+
+// Order-preserving key of (logit, expert id): the float's bits mapped so that unsigned order
+// is float order in the high word, the complemented id in the low word -- so the largest
+// key is the largest logit, ties going to the lower id.  0 marks an empty entry (every
+// finite logit maps above it).  -0 is keyed as +0: equal floats tie on the id.
+__device__ __forceinline__ unsigned long long route_key(float v, int e) {
+  const uint32_t b = v == 0.0f ? 0u : __float_as_uint(v);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (uint32_t)(~e);
+}
+__device__ __forceinline__ float key_logit(unsigned long long k) {
+  const uint32_t ord = (uint32_t)(k >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
 
 template <int EPL>  // experts per lane = ceil(E / 32)
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
@@ -29,49 +44,35 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     }
     return;
   }
-  float v[EPL];
-  bool live[EPL];
+  unsigned long long key[EPL];
   const float* row = logits + (size_t)t * E;
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = lane + 32 * j;
-    live[j] = e < E;
-    v[j] = live[j] ? row[e] : 0.0f;
+    key[j] = e < E ? route_key(row[e], e) : 0ull;
   }
   int my_id = -1;      // lane k keeps the k-th chosen id and logit
   float my_logit = 0.0f;
   float top_logit = 0.0f;
   for (int k = 0; k < K; ++k) {
-    // lane-local best: larger logit, then smaller id (ids grow with j)
-    float bv = 0.0f;
-    int bi = 0x7fffffff;
+    unsigned long long m = key[0];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      if (live[j] && (bi == 0x7fffffff || v[j] > bv)) {
-        bv = v[j];
-        bi = lane + 32 * j;
-      }
-    }
+    for (int j = 1; j < EPL; ++j) m = key[j] > m ? key[j] : m;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const bool take = (oi != 0x7fffffff) &&
-                        (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (take) {
-        bv = ov;
-        bi = oi;
-      }
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
+      m = o > m ? o : m;
     }
-    // bi / bv are now warp-uniform: the winner removes it
+    // m is warp-uniform: its owner clears it
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
-      if (lane + 32 * j == bi) live[j] = false;
+      if (key[j] == m) key[j] = 0ull;
+    const float lv = key_logit(m);
     if (lane == k) {
-      my_id = bi;
-      my_logit = bv;
+      my_id = (int)(~(uint32_t)m);
+      my_logit = lv;
     }
-    if (k == 0) top_logit = bv;
+    if (k == 0) top_logit = lv;
   }
   const float ex = (lane < K) ? expf(my_logit - top_logit) : 0.0f;
   // sum in ascending slot order (a fixed order, independent of the warp reduction tree)

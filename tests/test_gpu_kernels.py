@@ -61,7 +61,17 @@ def test_route_ties_and_small_shapes():
     assert np.array_equal(host(idx), oi)
     assert host(idx)[0].tolist() == [0, 1, 2, 3] and host(idx)[1].tolist() == [7, 33, 39, 0]
     assert np.allclose(host(wt), ow, rtol=1e-6)
-    for E, K in [(1, 1), (32, 32), (33, 5), (300, 6)]:
+    # signed zeros are equal logits: the lower id comes first
+    z = torch.zeros(2, 40, device="cuda")
+    z[0, [3, 9, 20]] = -0.0
+    z[0, [5, 11]] = 1.0
+    z[1, :] = -0.0
+    z[1, 17] = 0.0
+    idx, _ = moe.moe_route_topk(z, 4)
+    oi, _ = ref.route_topk(host(z), 4)
+    assert np.array_equal(host(idx), oi) and host(idx)[0].tolist() == [5, 11, 0, 1]
+    assert host(idx)[1].tolist() == [0, 1, 2, 3]
+    for E, K in [(1, 1), (32, 32), (33, 5), (300, 6), (1024, 8), (700, 32)]:
         lg = torch.randn(17, E, device="cuda", generator=torch.Generator("cuda").manual_seed(E))
         idx, wt = moe.moe_route_topk(lg, K)
         oi, ow = ref.route_topk(host(lg), K)

@@ -153,7 +153,25 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
     layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine, **kw)
-    st = dict(layer=layer, logits=logits, x=x,
+    fq = None
+    if w.fake_quant:
+        # combine fake-quant: the constant scale 448 / amax, amax calibrated (max) on a batch
+        # of 16 tokens drawn with seed + 1 through this layer's own weights (untimed)
+        wc = synth.scaled(w, T=16, T_valid=16, fake_quant=False, graph=False)
+        cal = moe.MoeLayer(wc.T, wc.H, wc.I, wc.E, wc.K, dtype, **kw)
+        c_idx = torch.empty(wc.T, wc.K, dtype=torch.int32, device=device)
+        c_wt = torch.empty(wc.T, wc.K, dtype=torch.float32, device=device)
+        c_out = torch.empty(wc.T, wc.H, dtype=torch.bfloat16, device=device)
+        cal.forward(synth.hidden(wc, seed + 1, device=device), c_out, c_idx, c_wt,
+                    logits=synth.router_logits(wc, seed + 1, device=device))
+        amax = torch.zeros(1, dtype=torch.float32, device=device)
+        cv = cal.views
+        moe.moe_combine_amax(cal.view("y", (cv.cap, wc.H), torch.bfloat16),
+                             cal.view("inv_map", (wc.T, wc.K), torch.int32), c_wt, amax)
+        fq = moe.moe_fq_scale_from_amax(amax)
+        torch.cuda.synchronize()
+        del cal
+    st = dict(layer=layer, fq=fq, logits=logits, x=x,
               idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
               wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
               out=torch.empty(w.T, w.H, dtype=torch.bfloat16, device=device),
@@ -165,7 +183,7 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
 def layer_step(st, x=None, logits=None, out=None):
     st["layer"].forward(st["x"] if x is None else x, st["out"] if out is None else out, st["idx"], st["wt"],
                         logits=st["logits"] if logits is None else logits, num_tokens=st["n"],
-                        dev_status=st["status"])
+                        fq_scale=st["fq"], dev_status=st["status"])
 
 
 STAGES = ("route", "permute", "gemm_gate_up", "gemm_down", "combine")
@@ -212,7 +230,7 @@ def staged_step(st, w, events):
         # down projection + combine in one launch: the combine stage below is empty
         assert L.moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m if mt else v.cu_seqlens, nseg, mt, v.cap,
                                           d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), d.dtype, v.y, None,
-                                          v.src_row, v.inv_map, p(st["wt"]), d.T, d.K, v.shared_map, None,
+                                          v.src_row, v.inv_map, p(st["wt"]), d.T, d.K, v.shared_map, p(st["fq"]),
                                           p(st["out"]), v.counters, p(st["status"]), s) == 0
         events[4].record()
         events[5].record()
@@ -227,7 +245,7 @@ def staged_step(st, w, events):
                                   s) == 0
     events[4].record()
     assert L.moe_combine(v.y, v.inv_map, p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None, v.shared_map,
-                         None, p(st["out"]), s) == 0
+                         p(st["fq"]), p(st["out"]), s) == 0
     events[5].record()
 
 
@@ -440,7 +458,9 @@ def run_ours(args, rank, world, local_rank):
                    "tokens_per_step": w.T_valid, "parallelism": f"token-sharded replicas x{world}",
                    "layout": (f"batched [{w.E + int(w.shared)}, {max_tokens}, H] + masked_m" if max_tokens
                               else "contiguous expert-major rows + cu_seqlens"),
-                   "combine": "fused into the down projection" if args.fuse_combine else "separate kernel",
+                   "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +
+                              (f", E4M3 fake-quant at the calibrated constant scale {float(st['fq'].item()):.5g}"
+                               if w.fake_quant else ""),
                    "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
         "gpu_launches": (sum(KERNELS_PER_STEP.values()) - int(args.fuse_combine)) * args.steps,
         "kernels": kernels,

@@ -13,7 +13,8 @@
 //
 // Every float op is an explicit round-to-nearest intrinsic (__fmul_rn / __fadd_rn /
 // __fdiv_rn) so the compiler cannot contract them into FMAs: the result is bit-exact
-// against a float32 reference fed the same rows.
+// against a float32 reference fed the same rows.  The fake-quant's division by s runs once
+// per E4M3 code into a shared-memory table, not once per element.
 //
 // One warp per (token, column part); lane l owns 16-byte vectors l, l+32, ... of the
 // part.  A token's row is split into `splits` parts only when there are too few tokens
@@ -40,6 +41,13 @@ __global__ void __launch_bounds__(256) combine_kernel(
   const int nvec = H / 8;
   const int per_part = SPLIT ? (nvec + splits - 1) / splits : nvec;
   const float s = FQ ? *fq_scale : 1.0f;
+  // fake-quant dequantisation table: code -> fl32(decode(code) / s), the same IEEE divisions
+  // the per-element QDQ would do (s is one scalar), made once per block
+  __shared__ float fq_tbl[FQ ? 256 : 1];
+  if (FQ) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) fq_tbl[i] = __fdiv_rn(e4m3_to_f32((uint8_t)i), s);
+    __syncthreads();
+  }
   float amax = 0.0f;
   bool mismatch = false;
   const int n_items = SPLIT ? T * splits : T;
@@ -84,7 +92,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
             amax = fmaxf(amax, fabsf(r));
             continue;
           }
-          if (FQ) r = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(r, s))), s);
+          if (FQ) r = fq_tbl[f32_to_e4m3(__fmul_rn(r, s))];
           acc[i] = __fadd_rn(acc[i], r);
         }
       }

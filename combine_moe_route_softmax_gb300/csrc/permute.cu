@@ -266,15 +266,16 @@ __device__ __forceinline__ int token_dest(const int32_t* __restrict__ inv_map, c
   return -1;
 }
 
-// Dispatch fake-quant of 8 BF16 values: bf16(e4m3(x * s) / s), float32 steps.
-__device__ __forceinline__ uint4 qdq8(const uint4 u, float s) {
+// Dispatch fake-quant of 8 BF16 values: bf16(e4m3(x * s) / s), float32 steps; the division
+// of each E4M3 code by s comes from a table made once per block (tbl[c] = decode(c) / s).
+__device__ __forceinline__ uint4 qdq8(const uint4 u, float s, const float* tbl) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-    const float ql = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(lo, s))), s);
-    const float qh = __fdiv_rn(e4m3_to_f32(f32_to_e4m3(__fmul_rn(hi, s))), s);
+    const float ql = tbl[f32_to_e4m3(__fmul_rn(lo, s))];
+    const float qh = tbl[f32_to_e4m3(__fmul_rn(hi, s))];
     o[i] = (uint32_t)f32_to_bf16(ql) | ((uint32_t)f32_to_bf16(qh) << 16);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -297,6 +298,11 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
   const int per_part = ((nvec + 127) / 128 + splits - 1) / splits * 128;   // vectors, whole groups
   const int ndst = K + 1;
   const float s = DQ ? *dq_scale : 1.0f;
+  __shared__ float dq_tbl[DQ ? 256 : 1];
+  if (DQ) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) dq_tbl[i] = __fdiv_rn(e4m3_to_f32((uint8_t)i), s);
+    __syncthreads();
+  }
   for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * splits; item += nw) {
     const int t = item / splits;
     const int v_begin = (item - t * splits) * per_part;
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
         const int v = v0 + lane + 32 * j;
         if (v < v_end) {
           r[j] = __ldg(in + v);
-          if (DQ) q[j] = qdq8(r[j], s);
+          if (DQ) q[j] = qdq8(r[j], s, dq_tbl);
         }
       }
       unsigned m = live;

@@ -347,11 +347,15 @@ def run_ours(args, rank, world, local_rank):
     # pipeline: the next batch's inputs are copied in (pinned host -> device, copy stream)
     # and the previous batch's output copied out (device -> pinned host, a second copy
     # stream) while the current batch computes; input and output buffers are doubled.
-    h_logits = st["logits"].cpu().pin_memory()
-    h_x = st["x"].cpu().pin_memory()
-    h_out = [torch.empty(st["out"].shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    d_logits = [torch.empty_like(st["logits"]) for _ in range(2)]
-    d_x = [torch.empty_like(st["x"]) for _ in range(2)]
+    # Only the batch's real tokens cross the host link: the bucket's padding rows (past
+    # num_tokens) are never read by the layer and always come out +0, so they stay on the
+    # device.
+    nv = w.T_valid
+    h_logits = st["logits"][:nv].cpu().pin_memory()
+    h_x = st["x"][:nv].cpu().pin_memory()
+    h_out = [torch.empty((nv, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_logits = [torch.zeros_like(st["logits"]) for _ in range(2)]
+    d_x = [torch.zeros_like(st["x"]) for _ in range(2)]
     d_out = [torch.empty_like(st["out"]) for _ in range(2)]
     comp = torch.cuda.current_stream()
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
@@ -364,8 +368,8 @@ def run_ours(args, rank, world, local_rank):
         h2d.wait_event(start)
         d2h.wait_event(start)
         with torch.cuda.stream(h2d):
-            d_logits[0].copy_(h_logits, non_blocking=True)
-            d_x[0].copy_(h_x, non_blocking=True)
+            d_logits[0][:nv].copy_(h_logits, non_blocking=True)
+            d_x[0][:nv].copy_(h_x, non_blocking=True)
             in_ready[0].record(h2d)
         for i in range(n):
             b = i % 2
@@ -380,13 +384,13 @@ def run_ours(args, rank, world, local_rank):
                 with torch.cuda.stream(h2d):
                     if comp_done[nb] is not None:
                         h2d.wait_event(comp_done[nb])  # step i-1 no longer reads this input set
-                    d_logits[nb].copy_(h_logits, non_blocking=True)
-                    d_x[nb].copy_(h_x, non_blocking=True)
+                    d_logits[nb][:nv].copy_(h_logits, non_blocking=True)
+                    d_x[nb][:nv].copy_(h_x, non_blocking=True)
                     in_ready[nb] = ev()
                     in_ready[nb].record(h2d)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(comp_done[b])
-                h_out[b].copy_(d_out[b], non_blocking=True)
+                h_out[b].copy_(d_out[b][:nv], non_blocking=True)
                 out_done[b] = ev()
                 out_done[b].record(d2h)
         for b in range(2):
@@ -406,7 +410,10 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
     assert st["status"].item() == 0
     # the pipelined run's last output reached the host intact (same batch, deterministic kernels)
-    assert torch.equal(h_out[(args.steps - 1) % 2], st["out"].cpu())
+    assert torch.equal(h_out[(args.steps - 1) % 2], st["out"][:nv].cpu())
+    # and the rows that stayed on the device are the bucket's +0 padding
+    last = d_out[(args.steps - 1) % 2]
+    assert not torch.any(last[nv:].view(torch.int16)), "padding rows of the bucket are not +0"
 
     if rank != 0:
         return
@@ -471,7 +478,9 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out[0].numel() * 2,
-                "pipeline": "inputs of step i+1 copied in and output of step i-1 copied out during step i"},
+                "pipeline": "inputs of step i+1 copied in and output of step i-1 copied out during step i; "
+                            "only the batch's real tokens cross the host link (bucket padding stays on the "
+                            "device)"},
         "graph": graph_line,
         "clocks": clocks,
         "cpu_baseline": cpu,

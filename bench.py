@@ -171,7 +171,9 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
         fq = moe.moe_fq_scale_from_amax(amax)
         torch.cuda.synchronize()
         del cal
-    st = dict(layer=layer, fq=fq, logits=logits, x=x,
+    # slot padding of the workload (a fixed seeded mask), applied by the harness after routing
+    pad = synth.slot_padding(w, seed, device=device) if w.slot_pad > 0 else None
+    st = dict(layer=layer, fq=fq, pad=pad, logits=logits, x=x,
               idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
               wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
               out=torch.empty(w.T, w.H, dtype=torch.bfloat16, device=device),
@@ -181,9 +183,17 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
 
 
 def layer_step(st, x=None, logits=None, out=None):
+    import combine_moe_route_softmax_gb300 as moe
+    lg = st["logits"] if logits is None else logits
+    if st["pad"] is not None:
+        # workloads with padded slots: route, then the harness marks its padding slots -1
+        # (weight 0), as a dispatcher would, and the layer runs on those ids
+        moe.moe_route_topk(lg, st["idx"].shape[1], num_tokens=st["n"], topk_idx=st["idx"], topk_w=st["wt"])
+        st["idx"].masked_fill_(st["pad"], -1)
+        st["wt"].masked_fill_(st["pad"], 0.0)
+        lg = None
     st["layer"].forward(st["x"] if x is None else x, st["out"] if out is None else out, st["idx"], st["wt"],
-                        logits=st["logits"] if logits is None else logits, num_tokens=st["n"],
-                        fq_scale=st["fq"], dev_status=st["status"])
+                        logits=lg, num_tokens=st["n"], fq_scale=st["fq"], dev_status=st["status"])
 
 
 STAGES = ("route", "permute", "gemm_gate_up", "gemm_down", "combine")
@@ -201,6 +211,9 @@ def staged_step(st, w, events):
     p = lambda t: None if t is None else t.data_ptr()
     events[0].record()
     assert L.moe_route_topk(p(st["logits"]), d.T, d.E, d.K, p(st["n"]), p(st["idx"]), p(st["wt"]), s) == 0
+    if st["pad"] is not None:
+        st["idx"].masked_fill_(st["pad"], -1)
+        st["wt"].masked_fill_(st["pad"], 0.0)
     events[1].record()
     mt = d.max_tokens
     if mt:
@@ -463,6 +476,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
                                f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
                    "tokens_per_step": w.T_valid, "parallelism": f"token-sharded replicas x{world}",
+                   "padding": (f"each slot -1 with p = {w.slot_pad} (the harness masks the routed ids)"
+                               if w.slot_pad > 0 else
+                               f"bucket rows >= {w.T_valid} (num_tokens on the device)" if w.T_valid < w.T
+                               else "none"),
                    "layout": (f"batched [{w.E + int(w.shared)}, {max_tokens}, H] + masked_m" if max_tokens
                               else "contiguous expert-major rows + cu_seqlens"),
                    "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +

@@ -17,9 +17,10 @@
 //           __match_any_sync ranks -> src_row / inv_map / shared_map (stable by slot)
 //           (batched layout: the row of rank r in segment e goes to e*max_tokens + r,
 //           ranks past max_tokens are dropped, and masked_m[e] = min(count, max_tokens))
-//   gather  source-ordered: one warp per token reads its row once (16-byte loads) and
-//           writes it to every row that holds it (the token's slots and its shared row),
-//           as BF16 or as E4M3 codes + 1x128 scales.  HBM-bound:
+//   gather  source-ordered: each token's row is read once and written to every row that
+//           holds it (the token's slots and its shared row): BF16 rows through TMA bulk
+//           copies staged in shared memory, E4M3 codes + 1x128 scales (or dispatch
+//           fake-quantised rows) through 16-byte vector loads and stores.  HBM-bound:
 //           T_valid*H*2 read + N*H*(2 | 1 + 4/128) written.
 #include "common.cuh"
 
@@ -338,6 +339,119 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
   }
 }
 
+// ------------------------------------------------------- TMA-staged gather (BF16 rows)
+// One bulk copy (cp.async.bulk) brings a token's row into shared memory; one bulk store per
+// destination row writes it out as a single contiguous transfer.  Each warp runs a two-deep
+// pipeline (the next token's row loads while the current one is stored); lane 0 issues the
+// copies, the warp shares the destination rows.  Waits on the load barriers are bounded
+// (2 s of globaltimer): on expiry the warp sets MOE_DEV_PIPELINE_TIMEOUT, waits (bounded)
+// for its load in flight and stops.
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t smem_u32addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bulk_row_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_row_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = gtimer();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (gtimer() - t0 > 2000000000ull) return false;
+  }
+}
+
+__global__ void __launch_bounds__(256) permute_gather_bf16_bulk_kernel(const uint16_t* __restrict__ x, int T, int K,
+                                                                       int H, const int32_t* __restrict__ inv_map,
+                                                                       const int32_t* __restrict__ shared_map,
+                                                                       uint16_t* __restrict__ xp,
+                                                                       int32_t* dev_status) {
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+  const uint32_t buf_stride = (row_bytes + 127) / 128 * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gsm);                       // [nwarps][2]
+  uint8_t* bufs = gsm + 128 + static_cast<size_t>(warp) * 2 * buf_stride;  // this warp's two rows
+  const uint32_t bar0 = smem_u32addr(bars + 2 * warp);
+  const uint32_t buf0 = smem_u32addr(bufs);
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const int ndst = K + 1;
+  const int nw = gridDim.x * nwarps;
+  // the next token (stride nw) that has a row to write, or T
+  auto next_live = [&](int t) {
+    for (; t < T; t += nw) {
+      const int d = token_dest(inv_map, shared_map, t, K, lane);
+      if (__ballot_sync(0xffffffffu, lane < ndst && d >= 0)) return t;
+    }
+    return T;
+  };
+  int cur = next_live(blockIdx.x * nwarps + warp);
+  int b = 0;
+  uint32_t phases = 0;              // bit i: parity of buffer i's next load
+  bool loading_next = false;        // a load into buffer b ^ 1 is in flight
+  if (lane == 0 && cur < T) bulk_row_load(buf0, x + (size_t)cur * H, row_bytes, bar0);
+  while (cur < T) {
+    const int nxt = next_live(cur + nw);
+    const int my_dst = token_dest(inv_map, shared_map, cur, K, lane);
+    const unsigned live = __ballot_sync(0xffffffffu, lane < ndst && my_dst >= 0);
+    const uint32_t nb = static_cast<uint32_t>(b ^ 1);
+    if (lane == 0 && nxt < T) {
+      // the stores of the token before `cur` read buffer nb: let them finish reading
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      bulk_row_load(buf0 + nb * buf_stride, x + (size_t)nxt * H, row_bytes, bar0 + 8 * nb);
+    }
+    loading_next = nxt < T;
+    bool ok = true;
+    if (lane == 0) ok = bulk_bar_wait(bar0 + 8 * b, (phases >> b) & 1u);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        if (dev_status) atomicOr(dev_status, MOE_DEV_PIPELINE_TIMEOUT);
+        if (loading_next) bulk_bar_wait(bar0 + 8 * nb, (phases >> nb) & 1u);
+      }
+      break;
+    }
+    phases ^= 1u << b;
+    unsigned m = live;
+    while (m) {
+      const int d = __ffs(m) - 1;
+      m &= m - 1;
+      const int row = __shfl_sync(0xffffffffu, my_dst, d);
+      if (lane == 0) bulk_row_store(xp + (size_t)row * H, buf0 + b * buf_stride, row_bytes);
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    cur = nxt;
+    b = static_cast<int>(nb);
+  }
+  // every store has been performed (and has read its row) before the warp leaves
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  __syncwarp();
+}
+
 // 1x128 quantisation of 8 elements per lane (a half-warp covers one 128-block): returns
 // the 8 codes packed in a uint2 and the block's scale.  Every lane of the warp calls it.
 __device__ __forceinline__ uint2 quant8(const uint4 u, bool live, float* scale) {
@@ -524,7 +638,22 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
   const long long items = (long long)T * splits;
   const int gblocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 8);
   const int32_t* smap = with_shared ? shared_map : nullptr;
-  if (out_dtype == MOE_BF16)
+  // BF16 rows without dispatch fake-quant: TMA-staged gather, one 8-warp block per SM (two
+  // row buffers per warp) when two rows per warp fit in shared memory
+  const size_t row_buf = ((size_t)H * 2 + 127) / 128 * 128;
+  const int bulk_warps = (int)std::min<size_t>(8, (232448 - 128) / (2 * row_buf));
+  if (out_dtype == MOE_BF16 && !dq_scale && bulk_warps >= 1) {
+    const size_t smem = 128 + (size_t)bulk_warps * 2 * row_buf;
+    static std::atomic<unsigned long long> attr_done{0};
+    if (!once_per_device(attr_done, [&] {
+          return cudaFuncSetAttribute(permute_gather_bf16_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      232448) == cudaSuccess;
+        }))
+      return MOE_ERR_CUDA;
+    const int blocks = std::max(1, std::min(num_sms(), (T + bulk_warps - 1) / bulk_warps));
+    permute_gather_bf16_bulk_kernel<<<blocks, bulk_warps * 32, smem, s>>>(x, T, K, H, inv_map, smap,
+                                                                          static_cast<uint16_t*>(xp), dev_status);
+  } else if (out_dtype == MOE_BF16)
     if (dq_scale)
       permute_gather_bf16_kernel<true><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
                                                                static_cast<uint16_t*>(xp), splits);

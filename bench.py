@@ -522,24 +522,35 @@ def oracle_sample(w, tokens, seed=0):
     return logits[toks], bits(x[:tokens]), w13, w2, shared
 
 
-def oracle_step(w, sample):
-    """The oracle's layer on the sample: route, permute, fp64 experts and the sum."""
+def oracle_step(w, sample, per_call=None):
+    """The oracle's layer on the sample: route, permute, fp64 experts and the sum (per-call
+    seconds accumulated into `per_call` when given)."""
     from oracle import moe_ref as ref
     logits, xb, w13, w2, shared = sample
+    t0 = time.perf_counter()
     idx, wt = ref.route_topk(logits, w.K)
+    t1 = time.perf_counter()
     ref.permute(idx, w.E, with_shared=w.shared)
-    return ref.layer_reference(xb, idx, wt, w13, w2, shared=shared)
+    t2 = time.perf_counter()
+    out = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared)
+    t3 = time.perf_counter()
+    if per_call is not None:
+        for k, v in (("route", t1 - t0), ("permute", t2 - t1), ("experts_and_sum", t3 - t2)):
+            per_call[k] = per_call.get(k, 0.0) + v
+    return out
 
 
 def cpu_baseline(w, tokens=8, reps=1):
     sample = oracle_sample(w, tokens)
+    per_call = {}
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle_step(w, sample)
+        oracle_step(w, sample, per_call)
     dt = (time.perf_counter() - t0) / reps
     return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{tokens} tokens of the {w.name} workload through the numpy oracle (route, permute, fp64 "
-                      f"experts, fixed-order sum); {dt:.1f} s"}
+                      f"experts, fixed-order sum); {dt:.1f} s",
+            "per_call_s": {k: round(v / reps, 4) for k, v in per_call.items()}}
 
 
 def run_reference(args, rank, world):

@@ -38,7 +38,9 @@ def make_layer(w, seed=0, fp8=False):
 
 
 @pytest.mark.parametrize("T,H,I,E,K,shared", [(1, 128, 128, 1, 1, False), (1, 256, 128, 4, 2, True),
-                                              (13, 384, 256, 3, 3, True), (200, 128, 384, 200, 1, False)])
+                                              (13, 384, 256, 3, 3, True), (200, 128, 384, 200, 1, False),
+                                              # top-k above 8: the 32-slot combine, wide permute scatter
+                                              (50, 256, 256, 64, 16, True), (20, 128, 128, 40, 32, False)])
 def test_degenerate_layers(T, H, I, E, K, shared):
     need_gpu()
     w = scaled(WORKLOADS["tiny"], T=T, T_valid=T, H=H, I=I, E=E, K=K, shared=shared)
@@ -154,3 +156,19 @@ def test_one_graph_replayed_at_every_bucket_fill():
         assert b["st"].item() == 0
         assert np.array_equal(bits(b["out"]), eager), n
         assert np.all(eager[n:] == 0) and np.all(host(b["idx"])[n:] == -1)
+
+
+def test_fp8_layer_with_twelve_experts_per_token():
+    """E4M3 layer with K = 12 and a shared expert against the oracle on the FP8 operands."""
+    need_gpu()
+    w = scaled(WORKLOADS["decode"], T=48, T_valid=48, H=512, I=256, E=32, K=12)
+    x, logits, (w13, w2, s13, s2), layer, b = make_layer(w, fp8=True)
+    layer.forward(x, b["out"], b["idx"], b["wt"], logits=logits, num_tokens=b["n"], dev_status=b["st"])
+    torch.cuda.synchronize()
+    assert b["st"].item() == 0
+    o_idx, o_w = ref.route_topk(host(logits), w.K)
+    assert np.array_equal(host(b["idx"]), o_idx)
+    want = ref.layer_reference(bits(x), o_idx, o_w, ExpertBits(w13), ExpertBits(w2), shared=(bits(s13), bits(s2)),
+                               fp8=True)
+    err = ref.max_rel_err(bf16_bits_to_f32(bits(b["out"])).astype(np.float64), want)
+    assert err <= 6e-2, err

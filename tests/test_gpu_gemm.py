@@ -47,6 +47,9 @@ CASES = [
     ([0, 128, 256], 256, 128, 256, 2, False),
     ([0, 0, 1, 1], 8, 512, 512, 3, False),
     ([0, 2500, 5000], 5000, 512, 1024, 2, False),
+    # CTA pairs on two M-tiles of one weight tile (2, 4 and 4 M-tiles, the second of a pair
+    # holding 2 rows or 1 row) next to a one-row segment (a pair of N-tiles)
+    ([0, 130, 130, 515, 1000, 1001], 1100, 256, 512, 4, True),
 ]
 
 

@@ -55,20 +55,41 @@ constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 constexpr int STAGE_OUT_PITCH = 80;                // 64 B of BF16 per row + 16 B pad (conflict-free)
 constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
 
+// Streamed segments (BF16, not fused): a segment of at most NS rows is computed by a
+// streaming CTA with the weights as the MMA's M operand (two M = 128 halves of a 256-row
+// weight tile) and the segment's rows as N = NS columns, through a deeper ring of
+// weight-sized stages.  Such a segment's units are bound by streaming their weights, and
+// one CTA keeps only four 32 KB weight tiles in flight behind 16 KB activation tiles that
+// hold a few real rows; here it keeps six behind 4 KB token tiles.
+constexpr int NS = 32;
+constexpr int YSTAGES = 6;
+constexpr int YT_BYTES = NS * KB_BYTES;
+constexpr int YSTAGE_BYTES = B_BYTES + YT_BYTES;   // 36 KB, a multiple of 1024
+
 struct SmemLayout {
+  // MMA-pipeline CTAs
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_BYTES;
-  static constexpr int bars = b + STAGES * B_BYTES;          // full[S], empty[S], tfull[2], tempty[2], drain
-  static constexpr int n_bars = 2 * STAGES + 5;
-  static constexpr int tmem_slot = bars + n_bars * 8;
+  static constexpr int xch = b + STAGES * B_BYTES;            // float [2][128]
+  static constexpr int stage_out = xch + 2 * 128 * 4;         // per epilogue warp: 32 x 80 B
+  static constexpr int x_end = stage_out + EPI_WARPS * STAGE_OUT_BYTES;
+  // streaming CTAs: YSTAGES x [256 weight rows | NS token rows]
+  static constexpr int y_end = YSTAGES * YSTAGE_BYTES;
+  // common tail at Args::common_off (after x_end, or after y_end when streaming is on):
+  // barriers full[6], empty[6], tfull[2], tempty[2], drain; TMEM slot; abort flag; role
+  // split; then int cu[nseg + 1], prefix[nseg + 1], prefix_y[nseg + 1]
+  static constexpr int n_bars = 2 * YSTAGES + 5;
+  static constexpr int tmem_slot = n_bars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
-  static constexpr int xch = abort_flag + 12;                 // float [2][128], 16-aligned
-  static constexpr int cu = xch + 2 * 128 * 4;                // int [MAX_SEG + 1]
-  static constexpr int prefix = cu + (MAX_SEG + 1) * 4;       // int [MAX_SEG + 1]
-  static constexpr int stage_out = (prefix + (MAX_SEG + 1) * 4 + 15) / 16 * 16;  // per epilogue warp: 32 x 80 B
-  static constexpr int end = stage_out + EPI_WARPS * STAGE_OUT_BYTES;
+  static constexpr int costs = abort_flag + 4;                // float [2]
+  static constexpr int arrays = 256;
+  static size_t bytes(int common_off, int nseg) {
+    return static_cast<size_t>(common_off) + arrays + ((3 * (nseg + 1) * 4 + 15) / 16) * 16 + 1024;  // + align slack
+  }
 };
-constexpr size_t SMEM_BYTES = SmemLayout::end + 1024;           // + alignment slack
+static_assert(SmemLayout::costs + 8 <= SmemLayout::arrays, "common tail header");
+static_assert(STAGES <= YSTAGES, "barrier slots");
+constexpr int SMEM_MAX = 227 * 1024;
 
 struct Args {
   const int32_t* cu;        // cu_seqlens [nseg + 1], or masked_m [nseg] when max_tokens > 0
@@ -95,6 +116,8 @@ struct Args {
   uint16_t* comb_out;       // [T, n_dim] BF16
   int32_t* counters;        // [T, n_dim / 128], zero on entry, left zero
   int T, K;
+  int stream;               // 1: segments of at most NS rows go to streaming CTAs
+  int common_off;           // shared-memory offset of the common tail
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -155,6 +178,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// With an L2 cache policy (createpolicy) attached to the copy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
 // Multicast variant: the box lands at the same shared-memory offset in every CTA of
 // cta_mask within the cluster and completes the transaction on each one's barrier there.
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
@@ -212,6 +244,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 16 consecutive float32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
@@ -231,6 +272,25 @@ __host__ __device__ constexpr uint32_t instr_desc() {
   return (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
+// BF16 x BF16 -> float32, M = 128 weight rows, N = NS token columns (streaming CTAs).
+__host__ __device__ constexpr uint32_t instr_desc_stream() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(NS >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+// Relative time of one unit (all units of a launch have the same K): an MMA-bound tile, a
+// single-tile segment's tile on the MMA pipeline, and a streamed unit.  They set how many
+// CTAs stream; measured per unit on the prefill expert mix with both roles running (gate/up:
+// 45.4 and 50.7 us; down: 12.9 and 14.8 us), the streamed cost rounded up so that the
+// streaming CTAs, which cannot hand work back, are not the last to finish.
+constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 53.5f;
+// Streaming CTAs: warp 0 loads the ring, warp 1 issues the MMAs, warps 2..5 are the
+// epilogue (one unit streams for tens of microseconds; its epilogue is short).
+constexpr int Y_EPI_WARPS = 4;
+// A streamed weight tile is read once: its copies carry an L2 evict-first policy, so the
+// streaming CTAs' gigabytes do not push out the weight tiles that the MMA pipeline's
+// M-tiles of one segment share through L2.
+constexpr bool STREAM_EVICT_FIRST = true;
 
 // SiLU with the fast exponential and divide: their relative error (a few 1e-6) is far
 // below the BF16 or E4M3 rounding of h that follows; for g < -87 the denominator exceeds
@@ -344,39 +404,128 @@ template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmBx, const __grid_constant__ CUtensorMap tmAh,
-                        const Args args) {
+                        const __grid_constant__ CUtensorMap tmAt, const Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars);
+  uint8_t* cmn = smem + args.common_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cmn);
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
-  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
-  auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
-  auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
-  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::tmem_slot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::abort_flag);
+  auto bar_empty = [&](int s) { return smem_u32(bars + YSTAGES + s); };
+  auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * YSTAGES + b); };
+  auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * YSTAGES + 2 + b); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * YSTAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cmn + SmemLayout::tmem_slot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(cmn + SmemLayout::abort_flag);
+  float* costs = reinterpret_cast<float*>(cmn + SmemLayout::costs);
   float* xch = reinterpret_cast<float*>(smem + SmemLayout::xch);
-  int* cu_s = reinterpret_cast<int*>(smem + SmemLayout::cu);
-  int* prefix = reinterpret_cast<int*>(smem + SmemLayout::prefix);
+  const int nseg = args.nseg;
+  int* cu_s = reinterpret_cast<int*>(cmn + SmemLayout::arrays);
+  int* prefix = cu_s + (nseg + 1);
+  int* prefix_y = prefix + (nseg + 1);
   uint8_t* stage_out = smem + SmemLayout::stage_out;
 
-  const int nseg = args.nseg;
   const int mtok = args.max_tokens;
   if (mtok > 0) {
     for (int i = tid; i < nseg; i += THREADS) cu_s[i] = i * mtok + min(max(args.cu[i], 0), mtok);
   } else {
     for (int i = tid; i <= nseg; i += THREADS) cu_s[i] = args.cu[i];
   }
+  __syncthreads();
+  const int n_tiles = SWIGLU ? (args.n_dim / 2) / 128 : (args.n_dim + BN - 1) / BN;
+  // per-segment counts -> exclusive prefixes (warp 0): M-tiles on the MMA pipeline, and
+  // streamed segments; plus the modelled time of each kind of work
+  if (warp == 0) {
+    const int chunk = (nseg + 31) / 32;
+    const int s0 = min(nseg, lane * chunk), s1 = min(nseg, s0 + chunk);
+    auto len = [&](int s) { return max(0, seg_end(cu_s, s, mtok) - seg_begin(cu_s, s, mtok)); };
+    // streaming pays only when every CTA has many units to spread (a static split of a
+    // handful of units per CTA is too coarse): at least 16 per CTA, from the M-tile count
+    bool stream_on = !FP8 && !FUSE && args.stream;
+    if (stream_on) {
+      int tiles = 0;
+      for (int s = s0; s < s1; ++s) tiles += (len(s) + BM - 1) / BM;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, off);
+      stream_on = static_cast<long long>(tiles) * n_tiles >= 16ll * gridDim.x;
+    }
+    auto streamed = [&](int l) { return stream_on && l > 0 && l <= NS; };
+    int local = 0, local_y = 0;
+    float cx = 0.0f, cy = 0.0f;
+    for (int s = s0; s < s1; ++s) {
+      const int l = len(s);
+      if (streamed(l)) {
+        ++local_y;
+        cy += COST_STREAM;
+      } else {
+        const int m = (l + BM - 1) / BM;
+        local += m;
+        cx += m == 1 ? COST_SINGLE : COST_MMA * static_cast<float>(m);
+      }
+    }
+    int incl = local, incl_y = local_y;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      const int vy = __shfl_up_sync(0xffffffffu, incl_y, off);
+      if (lane >= off) {
+        incl += v;
+        incl_y += vy;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      cx += __shfl_xor_sync(0xffffffffu, cx, off);
+      cy += __shfl_xor_sync(0xffffffffu, cy, off);
+    }
+    int run = incl - local, run_y = incl_y - local_y;
+    for (int s = s0; s < s1; ++s) {
+      prefix[s] = run;
+      prefix_y[s] = run_y;
+      const int l = len(s);
+      if (streamed(l))
+        ++run_y;
+      else
+        run += (l + BM - 1) / BM;
+    }
+    if (lane == 31) {
+      prefix[nseg] = incl;
+      prefix_y[nseg] = incl_y;
+    }
+    if (lane == 0) {
+      costs[0] = cx;
+      costs[1] = cy;
+    }
+  }
+  __syncthreads();
+  const int total_units = prefix[nseg] * n_tiles;
+  const int total_y = prefix_y[nseg] * n_tiles;
+  // CTAs [gx, gridDim.x) stream; every CTA derives the same split from the same counts.
+  // Pairs stay whole (both counts even), so no cluster straddles the two roles.
+  int ny = 0;
+  if (total_y > 0) {
+    const int G = gridDim.x, step = PAIR ? 2 : 1;
+    if (total_units == 0) {
+      ny = G;
+    } else {
+      const float f = costs[1] / (costs[0] + costs[1]);
+      ny = step * static_cast<int>(f * static_cast<float>(G) / static_cast<float>(step) + 0.5f);
+      ny = min(max(ny, step), G - step);
+    }
+  }
+  const int gx = static_cast<int>(gridDim.x) - ny;
+  const bool y_role = static_cast<int>(blockIdx.x) >= gx;
   if (tid == 64) {
-    for (int s = 0; s < STAGES; ++s) {
+    const int nst = y_role ? YSTAGES : STAGES;
+    for (int s = 0; s < nst; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), PAIR ? 2 : 1);   // PAIR: both CTAs' MMAs must release a stage
+      // PAIR (MMA pipeline): both CTAs' MMAs must release a stage
+      mbar_init(bar_empty(s), PAIR && !y_role ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
-      mbar_init(bar_tempty(b), EPI_WARPS);
+      mbar_init(bar_tempty(b), y_role ? Y_EPI_WARPS : EPI_WARPS);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -388,35 +537,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   // pair initialise theirs before either issues anything
   if (PAIR) cluster_sync_all();
   const uint32_t crank = PAIR ? cluster_ctarank() : 0;
-  // per-segment M-tile counts -> exclusive prefix (warp 0)
-  if (warp == 0) {
-    const int chunk = (nseg + 31) / 32;
-    const int s0 = min(nseg, lane * chunk), s1 = min(nseg, s0 + chunk);
-    int local = 0;
-    auto len = [&](int s) { return max(0, seg_end(cu_s, s, mtok) - seg_begin(cu_s, s, mtok)); };
-    for (int s = s0; s < s1; ++s) local += (len(s) + BM - 1) / BM;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int run = incl - local;
-    for (int s = s0; s < s1; ++s) {
-      prefix[s] = run;
-      run += (len(s) + BM - 1) / BM;
-    }
-    if (lane == 31) prefix[nseg] = incl;
-  }
-  __syncthreads();
-  const int n_tiles = SWIGLU ? (args.n_dim / 2) / 128 : (args.n_dim + BN - 1) / BN;
-  const int total_units = prefix[nseg] * n_tiles;
   if (FUSE && total_units == 0) {
     // no rows at all: every token's output is +0
     zero_rowless_tokens(args, blockIdx.x * (THREADS / 32) + warp, gridDim.x * (THREADS / 32), lane);
+    if (PAIR) cluster_sync_all();
     return;
   }
-  if (static_cast<int>(blockIdx.x) >= total_units) return;  // no work: nothing allocated yet
+  // no work: nothing allocated yet (both CTAs of a pair leave together, after the closing
+  // cluster barrier that the teardown would otherwise hold)
+  if (y_role ? static_cast<int>(blockIdx.x) - gx >= total_y : static_cast<int>(blockIdx.x) >= total_units) {
+    if (PAIR) cluster_sync_all();
+    return;
+  }
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -431,7 +563,176 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int KE = FP8 ? 128 : 64;  // K elements per stage
   const int kblocks = args.k_dim / KE;
 
-  if (warp == 0) {
+  if (y_role) {
+    if constexpr (!FP8 && !FUSE) {
+      // ================================================ streaming CTA: segments of <= NS rows
+      // Unit v: the t-th streamed segment (t = v / n_tiles) and N-tile nt = v % n_tiles.  The
+      // two 128-row halves of the weight tile are the A operands of two MMAs (M = 128) that
+      // share the segment's NS token rows as B (N = NS); TMEM buffer b holds half 0's
+      // products in columns [2 NS b, +NS) and half 1's in the next NS columns.
+      const int yi = static_cast<int>(blockIdx.x) - gx;
+      auto y_unit = [&](int v, int& seg, int& nt) {
+        const int t = v / n_tiles;
+        nt = v - t * n_tiles;
+        int lo = 0, hi = nseg - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix_y[mid] <= t)
+            lo = mid;
+          else
+            hi = mid - 1;
+        }
+        seg = lo;
+      };
+      if (warp == 0) {
+        if (lane == 0) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmAt)) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+          int stage = 0;
+          uint32_t phase = 0, armed = 0, last_parity = 0;
+          bool ok = true;
+          uint64_t wpol;
+          asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(wpol));
+          for (int v = yi; ok && v < total_y; v += ny) {
+            int seg, nt;
+            y_unit(v, seg, nt);
+            const int row0 = seg_begin(cu_s, seg, mtok);
+            const bool extra = seg >= args.num_w;
+            const CUtensorMap* mb = extra ? &tmBx : &tmB;
+            const int wbase = extra ? 0 : seg * args.n_dim;
+            const int rA = SWIGLU ? wbase + nt * 128 : wbase + nt * BN;
+            const int rB = SWIGLU ? wbase + args.n_dim / 2 + nt * 128 : rA + 128;
+            for (int kb = 0; kb < kblocks; ++kb) {
+              if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(bar_full(stage), YSTAGE_BYTES);
+              armed |= 1u << stage;
+              last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+              const uint32_t sw = sbase + stage * YSTAGE_BYTES;
+              if (STREAM_EVICT_FIRST) {
+                tma_load_2d_hint(sw, mb, kb * KE, rA, bar_full(stage), wpol);
+                tma_load_2d_hint(sw + B_HALF, mb, kb * KE, rB, bar_full(stage), wpol);
+              } else {
+                tma_load_2d(sw, mb, kb * KE, rA, bar_full(stage));
+                tma_load_2d(sw + B_HALF, mb, kb * KE, rB, bar_full(stage));
+              }
+              tma_load_2d(sw + B_BYTES, &tmAt, kb * KE, row0, bar_full(stage));
+              if (++stage == YSTAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+          if (!ok) {
+            for (int s = 0; s < YSTAGES; ++s)
+              if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
+          }
+        }
+      } else if (warp == 1) {
+        if (lane == 0) {
+          constexpr uint32_t idesc = instr_desc_stream();
+          int stage = 0, buf = 0;
+          uint32_t phase = 0, tphase = 0;
+          bool ok = true;
+          for (int v = yi; ok && v < total_y; v += ny) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+              if (kb == 0) {
+                if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t sw = sbase + stage * YSTAGE_BYTES;
+              const uint32_t st = sw + B_BYTES;
+              const uint32_t dt = tmem_base + buf * (2 * NS);
+#pragma unroll
+              for (int k = 0; k < KB_BYTES / 32; ++k) {
+                const uint32_t acc = (kb | k) != 0;
+                tc_mma<false>(dt, smem_desc(sw + 32 * k), smem_desc(st + 32 * k), idesc, acc);
+                tc_mma<false>(dt + NS, smem_desc(sw + B_HALF + 32 * k), smem_desc(st + 32 * k), idesc, acc);
+              }
+              tc_commit(bar_empty(stage));
+              if (++stage == YSTAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+              if (kb == kblocks - 1) {
+                tc_commit(bar_tfull(buf));
+                if (++buf == 2) {
+                  buf = 0;
+                  tphase ^= 1;
+                }
+              }
+            }
+          }
+          if (!ok) {
+            tc_commit(bar_drain);
+            mbar_drain(bar_drain, 0);
+          }
+        }
+      } else if (warp >= 2 && warp < 2 + Y_EPI_WARPS) {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4).. = weight rows j of both halves
+        const int q = warp & 3;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const int j = 32 * q + lane;
+        const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
+        int buf = 0;
+        uint32_t tphase = 0;
+        for (int v = yi; v < total_y; v += ny) {
+          int seg, nt;
+          y_unit(v, seg, nt);
+          const int row0 = seg_begin(cu_s, seg, mtok), row_end = seg_end(cu_s, seg, mtok);
+          if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status)) break;
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_addr + buf * (2 * NS);
+          uint32_t d0[NS], d1[NS];
+          tmem_ld32(tb, d0);
+          tmem_ld32(tb + NS, d1);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(buf));
+          if (++buf == 2) {
+            buf = 0;
+            tphase ^= 1;
+          }
+          const int rows = min(row_end - row0, NS);
+          if (SWIGLU) {
+            // gate row j in half 0, up row j in half 1: h[token, nt * 128 + j]
+            uint16_t* dst = static_cast<uint16_t*>(args.out) + (size_t)row0 * out_cols + nt * 128 + j;
+#pragma unroll
+            for (int n = 0; n < NS; ++n)
+              if (n < rows)
+                dst[(size_t)n * out_cols] = f32_to_bf16(silu(__uint_as_float(d0[n])) * __uint_as_float(d1[n]));
+          } else {
+            const int col = nt * BN + j;
+            uint16_t* dst = static_cast<uint16_t*>(args.out) + (size_t)row0 * out_cols + col;
+#pragma unroll
+            for (int n = 0; n < NS; ++n) {
+              if (n < rows) {
+                const float rs = args.row_scale ? args.row_scale[row0 + n] : 1.0f;
+                float v0 = __uint_as_float(d0[n]), v1 = __uint_as_float(d1[n]);
+                if (args.row_scale) {
+                  v0 = __fmul_rn(v0, rs);
+                  v1 = __fmul_rn(v1, rs);
+                }
+                if (col < out_cols) dst[(size_t)n * out_cols] = f32_to_bf16(v0);
+                if (col + 128 < out_cols) dst[(size_t)n * out_cols + 128] = f32_to_bf16(v1);
+              }
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -441,7 +742,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t armed = 0;  // bit s: stage s has been armed at least once
       uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < total_units; u += gx) {
         const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
         const bool extra = w.seg >= args.num_w;
         const CUtensorMap* mb = extra ? &tmBx : &tmB;
@@ -489,7 +790,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int buf = 0;
       uint32_t tphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < total_units; u += gx) {
         for (int kb = 0; kb < kblocks; ++kb) {
           const bool round_start = FP8 || kb == 0;
           if (round_start) {
@@ -547,10 +848,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
     if (FUSE) {
       // while the first accumulator fills: +0 rows for the tokens no unit will touch
-      const int active = min((int)gridDim.x, total_units);
+      const int active = min(gx, total_units);
       zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
     }
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total_units; u += gx) {
       const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
       const int row = w.row0 + r_in_tile;
       const bool row_ok = row < w.row_end;
@@ -790,18 +1091,17 @@ bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_
 
 template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
 moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
-                        const Args& args, int grid, cudaStream_t s) {
+                        const CUtensorMap& at, const Args& args, int grid, size_t smem, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR, FUSE>;
   static std::atomic<unsigned long long> attr_done{0};
   if (!once_per_device(attr_done, [&] {
-        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
-               cudaSuccess;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) == cudaSuccess;
       }))
     return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -810,7 +1110,7 @@ moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a, b, bx, ah, args) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, bx, ah, at, args) != cudaSuccess) return MOE_ERR_CUDA;
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -819,9 +1119,9 @@ moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 // CTAs of a pair always hold two n-tiles of one m-tile.
 template <bool FP8, bool SWIGLU, bool FUSE = false>
 moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
-                    const Args& args, int grid, bool pair, cudaStream_t s) {
-  if (pair) return launch_one<FP8, SWIGLU, true, FUSE>(a, b, bx, ah, args, grid & ~1, s);
-  return launch_one<FP8, SWIGLU, false, FUSE>(a, b, bx, ah, args, grid, s);
+                    const CUtensorMap& at, const Args& args, int grid, size_t smem, bool pair, cudaStream_t s) {
+  if (pair) return launch_one<FP8, SWIGLU, true, FUSE>(a, b, bx, ah, at, args, grid & ~1, smem, s);
+  return launch_one<FP8, SWIGLU, false, FUSE>(a, b, bx, ah, at, args, grid, smem, s);
 }
 
 }  // namespace gg
@@ -875,9 +1175,10 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
        reinterpret_cast<uintptr_t>(out)) & 15)
     return MOE_ERR_ARG;
   if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
-  CUtensorMap ma, mb, mbx, mah;
+  CUtensorMap ma, mb, mbx, mah, mat;
   if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
   if (!make_map(&mah, a, fp8, k_dim, rows_cap, BM / 2)) return MOE_ERR_CUDA;
+  if (!make_map(&mat, a, fp8, k_dim, rows_cap, NS)) return MOE_ERR_CUDA;
   const void* wb = num_w > 0 ? w : w_extra;
   const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
   if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
@@ -915,13 +1216,27 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
   const int grid = (int)std::min<long long>(num_sms(), max_units);
   const bool pair = n_tiles % 2 == 0 && grid >= 2;
+  // streaming CTAs for short segments: BF16, not fused, and a grid wide enough to split
+  bool stream_on = !fp8 && !fuse && grid >= 16;
+  int common_off = stream_on ? std::max(SmemLayout::x_end, SmemLayout::y_end) : SmemLayout::x_end;
+  size_t smem = SmemLayout::bytes(common_off, num_segments);
+  if (stream_on && smem > (size_t)SMEM_MAX) {
+    stream_on = false;
+    common_off = SmemLayout::x_end;
+    smem = SmemLayout::bytes(common_off, num_segments);
+  }
+  if (smem > (size_t)SMEM_MAX) return MOE_ERR_ARG;
+  args.stream = stream_on ? 1 : 0;
+  args.common_off = common_off;
   cudaStream_t s = as_stream(stream);
   if (fuse)
-    return fp8 ? launch<true, false, true>(ma, mb, mbx, mah, args, grid, pair, s)
-               : launch<false, false, true>(ma, mb, mbx, mah, args, grid, pair, s);
+    return fp8 ? launch<true, false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
+               : launch<false, false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
   if (fp8)
-    return swiglu ? launch<true, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<true, false>(ma, mb, mbx, mah, args, grid, pair, s);
-  return swiglu ? launch<false, true>(ma, mb, mbx, mah, args, grid, pair, s) : launch<false, false>(ma, mb, mbx, mah, args, grid, pair, s);
+    return swiglu ? launch<true, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
+                  : launch<true, false>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
+  return swiglu ? launch<false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
+                : launch<false, false>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
 }
 }  // namespace gg
 }  // namespace moe

@@ -137,3 +137,74 @@ def test_e4m3_block_scaled(case, swiglu):
         err = np.abs(got - want)
         assert np.all(err <= 2.0 ** -4 * np.abs(want) * 1.01 + srep * 2.0 ** -9 + 1e-3 * scale)
         assert np.all(host(out_s)[N:] == -1.0)
+
+
+def streamed_counts(seed, n_big, big_rows, n_small):
+    """Segment lengths: n_small segments of 1..32 rows (some empty) among n_big large ones."""
+    rng = np.random.default_rng(seed)
+    counts = list(rng.integers(0, 33, n_small)) + [big_rows + int(rng.integers(0, 100)) for _ in range(n_big)]
+    rng.shuffle(counts)
+    return [int(c) for c in counts]
+
+
+@pytest.mark.parametrize("swiglu", [True, False])
+@pytest.mark.parametrize("layout", ["contiguous", "batched"])
+def test_bf16_short_segments_on_streaming_ctas(swiglu, layout):
+    """Enough units per CTA that the launch splits its CTAs: segments of at most 32 rows go
+    to streaming CTAs (weights as the MMA's M operand, the segment's rows as N = 32), the
+    rest to the MMA pipeline.  Covers a short extra (shared-expert) segment, empty segments,
+    row_scale on the plain epilogue, and the batched layout's masked_m bounds."""
+    need_gpu()
+    k = 256
+    n = 4096 if swiglu else 2048        # 16 or 8 N-tiles: >= 16 units per CTA on 152 SMs
+    if layout == "contiguous":
+        counts = streamed_counts(7 + swiglu, 9 if swiglu else 10, 2000 if swiglu else 3900, 60)
+    else:
+        counts = streamed_counts(9 + swiglu, 12 if swiglu else 34, 900, 60)
+    counts.append(20)                   # the extra segment, short: streamed from w_extra
+    num_w = len(counts) - 1
+    S = len(counts)
+    g = torch.Generator().manual_seed(11)
+    w = (torch.randn(num_w, n, k, generator=g) / k ** 0.5).to(torch.bfloat16)
+    wx = (torch.randn(n, k, generator=g) / k ** 0.5).to(torch.bfloat16)
+    cols = n // 2 if swiglu else n
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f = lambda b: bf16_bits_to_f32(b).astype(np.float64)
+    epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE
+    if layout == "contiguous":
+        cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        rows = int(cu[-1])
+        a = torch.randn(rows, k, generator=g).to(torch.bfloat16)
+        rs = None if swiglu else torch.rand(rows, generator=g) + 0.5
+        out = torch.full((rows, cols), SENTINEL, dtype=torch.int16).view(torch.bfloat16).cuda()
+        moe.moe_grouped_gemm(a.cuda(), torch.from_numpy(cu).cuda(), w.cuda(), w_extra=wx.cuda(), epilogue=epi,
+                             out=out, dev_status=st, row_scale=None if rs is None else rs.cuda())
+        spans = [(int(cu[s]), int(cu[s + 1]), int(cu[s + 1])) for s in range(S)]
+    else:
+        mt = 1024
+        a = torch.randn(S, mt, k, generator=g).to(torch.bfloat16)
+        rs = None if swiglu else torch.rand(S * mt, generator=g) + 0.5
+        out = torch.full((S, mt, cols), SENTINEL, dtype=torch.int16).view(torch.bfloat16).cuda()
+        moe.moe_grouped_gemm_batched(a.cuda(), torch.tensor(counts, dtype=torch.int32).cuda(), w.cuda(),
+                                     w_extra=wx.cuda(), epilogue=epi, out=out, dev_status=st,
+                                     row_scale=None if rs is None else rs.cuda())
+        spans = [(s * mt, s * mt + counts[s], (s + 1) * mt) for s in range(S)]
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ob = bits(out).reshape(-1, cols)
+    ab = bits(a).reshape(-1, k)
+    w64, wx64 = f(bits(w)), f(bits(wx))
+    for s, (b, e, cap) in enumerate(spans):
+        assert np.all(ob[e:cap] == SENTINEL)          # rows past a batched segment's count
+        if e == b:
+            continue
+        acc = f(ab[b:e]) @ (w64[s] if s < num_w else wx64).T
+        if swiglu:
+            I = acc.shape[1] // 2
+            with np.errstate(over="ignore"):
+                acc = acc[:, :I] / (1.0 + np.exp(-acc[:, :I])) * acc[:, I:]
+        elif rs is not None:
+            acc = acc * rs.numpy().astype(np.float64)[b:e, None]
+        scale = np.abs(acc).max()
+        err = np.abs(f(ob[b:e]) - acc)
+        assert np.all(err <= 2.0 ** -8 * np.abs(acc) + 2e-3 * scale), (s, e - b, err.max() / scale)

@@ -1,6 +1,6 @@
 // Grouped GEMM over the expert segments on the 5th-generation tensor cores (sm_103a):
 // tcgen05.mma with accumulators in tensor memory (TMEM), operands staged in shared memory
-// by TMA (cp.async.bulk.tensor, 128-byte swizzle, no multicast), and a persistent
+// by TMA (cp.async.bulk.tensor, 128-byte swizzle), and a persistent
 // per-expert tile scheduler that builds its tile list on the device from cu_seqlens, so
 // the host never needs the segment lengths (no host sync; graph-capturable).
 //
@@ -13,7 +13,18 @@
 // of a tile are 128 gate rows and the matching 128 up rows, so one MMA with N = 256
 // yields g and u for 128 output columns side by side in TMEM.
 //
-// Warp roles (320 threads, one CTA per SM):
+// CTA pairs (clusters of 2, when the N-tile count is even): the two CTAs hold two N-tiles
+// of one M-tile, each fetches half of the shared activation rows and multicasts them.
+//
+// Two roles.  The MMA pipeline below takes every segment when streaming is off, and the
+// segments of more than NS = 32 rows when it is on.  Streaming CTAs (the last ny CTAs of
+// the grid, BF16 and not fused, when the launch has at least 16 units per CTA) take the
+// segments of at most NS rows: such a segment is a weight stream, so its CTAs keep six
+// 32 KB weight tiles in flight behind 4 KB token tiles and issue MMAs with the weights as
+// the M = 128 operand and the segment's rows as N = NS.  Every CTA derives the same ny from
+// the segment lengths and a per-unit cost model, so no host sync is needed.
+//
+// Warp roles of the MMA pipeline (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator + MMA issuer (one lane)
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (its subpartition) and

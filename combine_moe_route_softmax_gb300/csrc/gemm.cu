@@ -527,6 +527,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   const int gx = static_cast<int>(gridDim.x) - ny;
   const bool y_role = static_cast<int>(blockIdx.x) >= gx;
+  // MMA-pipeline CTAs actually used: the fewest (in whole pairs) that keep the largest
+  // per-CTA unit count, so the last round of units is full instead of a few CTAs finishing
+  // alone (weight-streaming launches such as decode, where those few cannot draw the HBM
+  // bandwidth that all of them share); compute-bound launches keep their critical path.
+  int gxu = gx;
+  if (total_units > 0 && gx > 0) {
+    const int step = PAIR ? 2 : 1;
+    const int per = (total_units + gx - 1) / gx;
+    gxu = min(gx, ((total_units + per - 1) / per + step - 1) / step * step);
+  }
   if (tid == 64) {
     const int nst = y_role ? YSTAGES : STAGES;
     for (int s = 0; s < nst; ++s) {
@@ -556,7 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   // no work: nothing allocated yet (both CTAs of a pair leave together, after the closing
   // cluster barrier that the teardown would otherwise hold)
-  if (y_role ? static_cast<int>(blockIdx.x) - gx >= total_y : static_cast<int>(blockIdx.x) >= total_units) {
+  if (y_role ? static_cast<int>(blockIdx.x) - gx >= total_y
+             : static_cast<int>(blockIdx.x) >= min(total_units, gxu)) {
     if (PAIR) cluster_sync_all();
     return;
   }
@@ -753,7 +764,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t armed = 0;  // bit s: stage s has been armed at least once
       uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gx) {
+      for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
         const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
         const bool extra = w.seg >= args.num_w;
         const CUtensorMap* mb = extra ? &tmBx : &tmB;
@@ -801,7 +812,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int buf = 0;
       uint32_t tphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gx) {
+      for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
         for (int kb = 0; kb < kblocks; ++kb) {
           const bool round_start = FP8 || kb == 0;
           if (round_start) {
@@ -859,10 +870,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int out_cols = SWIGLU ? args.n_dim / 2 : args.n_dim;
     if (FUSE) {
       // while the first accumulator fills: +0 rows for the tokens no unit will touch
-      const int active = min(gx, total_units);
+      const int active = min(gxu, total_units);
       zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
     }
-    for (int u = blockIdx.x; u < total_units; u += gx) {
+    for (int u = blockIdx.x; u < total_units; u += gxu) {
       const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
       const int row = w.row0 + r_in_tile;
       const bool row_ok = row < w.row_end;

@@ -319,11 +319,18 @@ __device__ __forceinline__ int seg_begin(const int* bnd, int s, int max_tokens) 
 __device__ __forceinline__ int seg_end(const int* bnd, int s, int max_tokens) {
   return max_tokens > 0 ? bnd[s] : bnd[s + 1];
 }
+// Unit order within a segment: groups of `mgroup` M-tiles; inside a group, for each pair of
+// N-tiles (one N-tile when the count is odd) every M-tile of the group in turn.  A round of
+// the grid then holds a few weight tiles read by many M-tiles, so a large expert's weights
+// cross HBM about once per group instead of once per round, while two consecutive units
+// still share an M-tile (CTA pairs multicast its rows).  mgroup = 0: M-tile-major order.
+// Used for the BF16 gate/up (7168-deep K: a weight tile is 3.7 MB); the down projection's
+// short units ran slower grouped (1.86 against 1.83 ms) and keep the M-tile-major order.
+constexpr int MGROUP_GATE_UP = 32;
 __device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, const int* prefix, int nseg,
-                                            int max_tokens) {
+                                            int max_tokens, int mgroup) {
   Unit w;
   const int mt = u / n_tiles;
-  w.nt = u - mt * n_tiles;
   int lo = 0, hi = nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -333,7 +340,24 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, c
       hi = mid - 1;
   }
   w.seg = lo;
-  w.row0 = seg_begin(cu, lo, max_tokens) + (mt - prefix[lo]) * BM;
+  int lm;
+  if (mgroup == 0) {
+    lm = mt - prefix[lo];
+    w.nt = u - mt * n_tiles;
+  } else {
+    const int m = prefix[lo + 1] - prefix[lo];
+    const int l = u - prefix[lo] * n_tiles;
+    const int g = l / (mgroup * n_tiles);
+    const int gs = min(mgroup, m - g * mgroup);
+    const int r = l - g * mgroup * n_tiles;
+    const int npw = (n_tiles & 1) ? 1 : 2;
+    const int chunk = npw * gs;
+    const int np = r / chunk;
+    const int rr = r - np * chunk;
+    lm = g * mgroup + rr / npw;
+    w.nt = np * npw + (rr - (rr / npw) * npw);
+  }
+  w.row0 = seg_begin(cu, lo, max_tokens) + lm * BM;
   w.row_end = seg_end(cu, lo, max_tokens);
   return w;
 }
@@ -765,7 +789,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
-        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
+        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok, SWIGLU && !FP8 ? MGROUP_GATE_UP : 0);
         const bool extra = w.seg >= args.num_w;
         const CUtensorMap* mb = extra ? &tmBx : &tmB;
         const int wbase = extra ? 0 : w.seg * args.n_dim;
@@ -874,7 +898,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
     }
     for (int u = blockIdx.x; u < total_units; u += gxu) {
-      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok);
+      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok, SWIGLU && !FP8 ? MGROUP_GATE_UP : 0);
       const int row = w.row0 + r_in_tile;
       const bool row_ok = row < w.row_end;
       // first output column this thread covers and whether that 128-column block exists

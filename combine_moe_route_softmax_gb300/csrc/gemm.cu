@@ -1107,8 +1107,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------------- host side
-// The driver's tensor-map encoder, looked up once (a function-local static: thread-safe
-// initialisation when several host threads make their first call together).
+// cuTensorMapEncodeTiled from the CUDA driver API, looked up once (a function-local static:
+// thread-safe initialisation when several host threads make their first call together).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;

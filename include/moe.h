@@ -42,7 +42,7 @@ typedef enum {
   MOE_OK = 0,
   MOE_ERR_ARG = 1,          /* bad size or null required pointer (host-side, nothing launched) */
   MOE_ERR_WORKSPACE = 2,    /* workspace smaller than the size query returns */
-  MOE_ERR_UNSUPPORTED = 3,  /* valid request this build does not implement */
+  MOE_ERR_UNSUPPORTED = 3,  /* valid request the library does not implement */
   MOE_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
 } moe_status_t;
 

@@ -135,7 +135,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
+def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -171,9 +171,19 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False):
         fq = moe.moe_fq_scale_from_amax(amax)
         torch.cuda.synchronize()
         del cal
+    dq = None
+    if dispatch_fq:
+        # dispatch fake-quant: the per-tensor scale 448 / max|x| over the batch's real tokens
+        # (untimed, as a calibration would be)
+        if w.dtype != "bf16":
+            raise SystemExit("--dispatch-fq applies to BF16 workloads (E4M3 rows are quantised anyway)")
+        amax = torch.zeros(1, dtype=torch.float32, device=device)
+        moe.moe_amax_bf16(x[:w.T_valid], amax)
+        dq = moe.moe_fq_scale_from_amax(amax)
+        torch.cuda.synchronize()
     # slot padding of the workload (a fixed seeded mask), applied by the harness after routing
     pad = synth.slot_padding(w, seed, device=device) if w.slot_pad > 0 else None
-    st = dict(layer=layer, fq=fq, pad=pad, logits=logits, x=x,
+    st = dict(layer=layer, fq=fq, dq=dq, pad=pad, logits=logits, x=x,
               idx=torch.empty(w.T, w.K, dtype=torch.int32, device=device),
               wt=torch.empty(w.T, w.K, dtype=torch.float32, device=device),
               out=torch.empty(w.T, w.H, dtype=torch.bfloat16, device=device),
@@ -193,7 +203,8 @@ def layer_step(st, x=None, logits=None, out=None):
         st["wt"].masked_fill_(st["pad"], 0.0)
         lg = None
     st["layer"].forward(st["x"] if x is None else x, st["out"] if out is None else out, st["idx"], st["wt"],
-                        logits=lg, num_tokens=st["n"], fq_scale=st["fq"], dev_status=st["status"])
+                        logits=lg, num_tokens=st["n"], fq_scale=st["fq"], dev_status=st["status"],
+                        dispatch_scale=st["dq"])
 
 
 STAGES = ("route", "permute", "gemm_gate_up", "gemm_down", "combine")
@@ -224,7 +235,11 @@ def staged_step(st, w, events):
     if mt:
         assert L.moe_permute_batched(p(st["idx"]), d.T, d.K, d.E, d.has_shared, mt, p(st["x"]), d.H, d.dtype, v.xp,
                                      v.xp_scales, v.masked_m, v.src_row, v.inv_map, v.shared_map, p(scratch),
-                                     scratch_bytes, p(st["status"]), None, None, None, s) == 0
+                                     scratch_bytes, p(st["status"]), p(st["dq"]), None, None, s) == 0
+    elif st["dq"] is not None:
+        assert L.moe_permute_ex(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
+                                v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
+                                scratch_bytes, p(st["status"]), p(st["dq"]), None, None, s) == 0
     else:
         assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
                              v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
@@ -299,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
     dist_init(world, "nccl")
     w = synth.WORKLOADS[args.workload]
     max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
-    st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine)
+    st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine, args.dispatch_fq)
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -459,7 +474,8 @@ def run_ours(args, rank, world, local_rank):
         with open(tr_path) as f:
             key = args.workload + ("/batched" if max_tokens else "")
             traffic = json.load(f).get(f"{key}:{dom}")
-    cpu = cpu_baseline(w, tokens=args.cpu_tokens) if world == 1 and not args.no_cpu_baseline else None
+    cpu = (cpu_baseline(w, tokens=args.cpu_tokens, dispatch_fq=args.dispatch_fq)
+           if world == 1 and not args.no_cpu_baseline else None)
     line = {
         "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
         "value": round(tok / (ms * 1e-3), 1),
@@ -485,6 +501,9 @@ def run_ours(args, rank, world, local_rank):
                    "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +
                               (f", E4M3 fake-quant at the calibrated constant scale {float(st['fq'].item()):.5g}"
                                if w.fake_quant else ""),
+                   "dispatch": (f"E4M3 fake-quant of the routed experts' rows at the per-tensor scale "
+                                f"{float(st['dq'].item()):.5g} (448 / max|x|)" if st["dq"] is not None
+                                else "rows as they are"),
                    "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
         "gpu_launches": (sum(KERNELS_PER_STEP.values()) - int(args.fuse_combine)) * args.steps,
         "kernels": kernels,
@@ -522,9 +541,10 @@ def oracle_sample(w, tokens, seed=0):
     return logits[toks], bits(x[:tokens]), w13, w2, shared
 
 
-def oracle_step(w, sample, per_call=None):
+def oracle_step(w, sample, per_call=None, dispatch_fq=False):
     """The oracle's layer on the sample: route, permute, fp64 experts and the sum (per-call
-    seconds accumulated into `per_call` when given)."""
+    seconds accumulated into `per_call` when given).  dispatch_fq: the routed experts see
+    the sample's rows fake-quantised at the oracle's own per-tensor scale."""
     from oracle import moe_ref as ref
     logits, xb, w13, w2, shared = sample
     t0 = time.perf_counter()
@@ -532,7 +552,8 @@ def oracle_step(w, sample, per_call=None):
     t1 = time.perf_counter()
     ref.permute(idx, w.E, with_shared=w.shared)
     t2 = time.perf_counter()
-    out = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared)
+    dq = ref.fq_scale_from_amax(ref.tensor_amax(xb)) if dispatch_fq else None
+    out = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared, dispatch_scale=dq)
     t3 = time.perf_counter()
     if per_call is not None:
         for k, v in (("route", t1 - t0), ("permute", t2 - t1), ("experts_and_sum", t3 - t2)):
@@ -540,12 +561,12 @@ def oracle_step(w, sample, per_call=None):
     return out
 
 
-def cpu_baseline(w, tokens=8, reps=1):
+def cpu_baseline(w, tokens=8, reps=1, dispatch_fq=False):
     sample = oracle_sample(w, tokens)
     per_call = {}
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle_step(w, sample, per_call)
+        oracle_step(w, sample, per_call, dispatch_fq)
     dt = (time.perf_counter() - t0) / reps
     return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{tokens} tokens of the {w.name} workload through the numpy oracle (route, permute, fp64 "
@@ -559,10 +580,10 @@ def run_reference(args, rank, world):
     w = synth.WORKLOADS[args.workload]
     sample = oracle_sample(w, args.ref_tokens)
     for _ in range(args.warmup):
-        oracle_step(w, sample)
+        oracle_step(w, sample, None, args.dispatch_fq)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(w, sample)
+        oracle_step(w, sample, None, args.dispatch_fq)
     dt = (time.perf_counter() - t0) / args.steps
     v = round(args.ref_tokens / dt, 3)
     line = {
@@ -573,7 +594,9 @@ def run_reference(args, rank, world):
         "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
                                f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
-                   "tokens_per_step": args.ref_tokens},
+                   "tokens_per_step": args.ref_tokens,
+                   "dispatch": ("E4M3 fake-quant of the routed experts' rows at the per-tensor scale 448 / max|x|"
+                                if args.dispatch_fq else "rows as they are")},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "kind": "oracle", "cores": os.cpu_count(),
                          "sample": f"{args.ref_tokens} tokens per step through the numpy oracle"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -593,6 +616,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["contiguous", "batched"], default="contiguous",
                     help="expert-major rows with cu_seqlens, or the batched [E, max_tokens, H] layout")
+    ap.add_argument("--dispatch-fq", action="store_true",
+                    help="BF16 workloads: E4M3 fake-quant of the routed experts' input rows (per-tensor scale)")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="run the combine inside the down projection (moe_grouped_gemm_combine)")
     ap.add_argument("--max-tokens", type=int, default=0,

@@ -135,7 +135,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=False):
+def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=False, weight_in_down=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -152,7 +152,8 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
             kw.update(shared_w13=qs13, shared_w2=qs2, shared_w13_scales=cs13, shared_w2_scales=cs2)
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
-    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine, **kw)
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine,
+                         weight_in_down=weight_in_down, **kw)
     fq = None
     if w.fake_quant:
         # combine fake-quant: the constant scale 448 / amax, amax calibrated (max) on a batch
@@ -227,6 +228,10 @@ def staged_step(st, w, events):
         st["wt"].masked_fill_(st["pad"], 0.0)
     events[1].record()
     mt = d.max_tokens
+    # router weight in the down projection: the permute emits each row's weight, the down
+    # GEMM scales its accumulator by it and the combine only sums
+    wd = bool(d.weight_in_down)
+    wd_w, wd_rows = (p(st["wt"]), v.row_weights) if wd else (None, None)
     if mt:
         scratch_bytes = L.moe_permute_batched_workspace_bytes(d.T, d.K, d.E, d.has_shared)
     else:
@@ -235,11 +240,11 @@ def staged_step(st, w, events):
     if mt:
         assert L.moe_permute_batched(p(st["idx"]), d.T, d.K, d.E, d.has_shared, mt, p(st["x"]), d.H, d.dtype, v.xp,
                                      v.xp_scales, v.masked_m, v.src_row, v.inv_map, v.shared_map, p(scratch),
-                                     scratch_bytes, p(st["status"]), p(st["dq"]), None, None, s) == 0
-    elif st["dq"] is not None:
+                                     scratch_bytes, p(st["status"]), p(st["dq"]), wd_w, wd_rows, s) == 0
+    elif st["dq"] is not None or wd:
         assert L.moe_permute_ex(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
                                 v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
-                                scratch_bytes, p(st["status"]), p(st["dq"]), None, None, s) == 0
+                                scratch_bytes, p(st["status"]), p(st["dq"]), wd_w, wd_rows, s) == 0
     else:
         assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
                              v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
@@ -257,8 +262,9 @@ def staged_step(st, w, events):
     if d.fuse_combine:
         # down projection + combine in one launch: the combine stage below is empty
         assert L.moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m if mt else v.cu_seqlens, nseg, mt, v.cap,
-                                          d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), d.dtype, v.y, None,
-                                          v.src_row, v.inv_map, p(st["wt"]), d.T, d.K, v.shared_map, p(st["fq"]),
+                                          d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), d.dtype, v.y, wd_rows,
+                                          v.src_row, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, v.shared_map,
+                                          p(st["fq"]),
                                           p(st["out"]), v.counters, p(st["status"]), s) == 0
         events[4].record()
         events[5].record()
@@ -266,14 +272,14 @@ def staged_step(st, w, events):
     if mt:
         assert L.moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, nseg, mt, d.I, d.H, p(tw[1]), p(tw[5]),
                                           d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None,
-                                          p(st["status"]), None, s) == 0
+                                          p(st["status"]), wd_rows, s) == 0
     else:
-        assert L.moe_grouped_gemm(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]),
-                                  d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
-                                  s) == 0
+        assert L.moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]),
+                                     d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
+                                     wd_rows, s) == 0
     events[4].record()
-    assert L.moe_combine(v.y, v.inv_map, p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None, v.shared_map,
-                         p(st["fq"]), p(st["out"]), s) == 0
+    assert L.moe_combine(v.y, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None,
+                         v.shared_map, p(st["fq"]), p(st["out"]), s) == 0
     events[5].record()
 
 
@@ -314,7 +320,8 @@ def run_ours(args, rank, world, local_rank):
     dist_init(world, "nccl")
     w = synth.WORKLOADS[args.workload]
     max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
-    st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine, args.dispatch_fq)
+    st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine, args.dispatch_fq,
+                        args.weight_in_down)
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -336,6 +343,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = clk.summary()
 
     # --- timed region 2: per-kernel breakdown (same kernels, events between the calls)
+    layer_out = st["out"].clone()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -343,6 +351,8 @@ def run_ours(args, rank, world, local_rank):
         staged_step(st, w, ev[i])
     torch.cuda.synchronize()
     barrier(world)
+    # the call-by-call step is the layer's computation: same output bit for bit
+    assert torch.equal(st["out"].view(torch.int16), layer_out.view(torch.int16)), "staged step differs from the layer"
     stage_ms = {}
     for j, name in enumerate(STAGES):
         t = statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
@@ -501,6 +511,8 @@ def run_ours(args, rank, world, local_rank):
                    "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +
                               (f", E4M3 fake-quant at the calibrated constant scale {float(st['fq'].item()):.5g}"
                                if w.fake_quant else ""),
+                   "router_weight": ("applied in the down projection's epilogue (weighted rows; the combine sums)"
+                                     if args.weight_in_down else "applied in the combine"),
                    "dispatch": (f"E4M3 fake-quant of the routed experts' rows at the per-tensor scale "
                                 f"{float(st['dq'].item()):.5g} (448 / max|x|)" if st["dq"] is not None
                                 else "rows as they are"),
@@ -616,6 +628,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["contiguous", "batched"], default="contiguous",
                     help="expert-major rows with cu_seqlens, or the batched [E, max_tokens, H] layout")
+    ap.add_argument("--weight-in-down", action="store_true",
+                    help="apply the router weights in the down projection's epilogue (the combine only sums)")
     ap.add_argument("--dispatch-fq", action="store_true",
                     help="BF16 workloads: E4M3 fake-quant of the routed experts' input rows (per-tensor scale)")
     ap.add_argument("--fuse-combine", action="store_true",

@@ -147,20 +147,28 @@ def streamed_counts(seed, n_big, big_rows, n_small):
     return [int(c) for c in counts]
 
 
-@pytest.mark.parametrize("swiglu", [True, False])
-@pytest.mark.parametrize("layout", ["contiguous", "batched"])
-def test_bf16_short_segments_on_streaming_ctas(swiglu, layout):
+STREAM_CASES = [
+    # swiglu, layout, n (weight rows), big segments, their rows
+    (True, "contiguous", 4096, 9, 2000),      # 16 N-tiles: CTA pairs
+    (False, "contiguous", 2048, 10, 3900),    # 8 N-tiles
+    (True, "batched", 4096, 12, 900),
+    (False, "batched", 2048, 34, 900),
+    (True, "contiguous", 2816, 10, 2100),     # 11 N-tiles: no pairs, an odd streaming CTA count allowed
+    (False, "contiguous", 2176, 10, 3000),    # 9 N-tiles, the last one half outside the weights
+]
+
+
+@pytest.mark.parametrize("swiglu,layout,n,n_big,big_rows", STREAM_CASES,
+                         ids=[f"{'swiglu' if c[0] else 'plain'}-{c[1]}-n{c[2]}" for c in STREAM_CASES])
+def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_rows):
     """Enough units per CTA that the launch splits its CTAs: segments of at most 32 rows go
     to streaming CTAs (weights as the MMA's M operand, the segment's rows as N = 32), the
     rest to the MMA pipeline.  Covers a short extra (shared-expert) segment, empty segments,
-    row_scale on the plain epilogue, and the batched layout's masked_m bounds."""
+    row_scale on the plain epilogue, the batched layout's masked_m bounds, odd N-tile counts
+    (no CTA pairs) and a last N-tile that reaches past the weight rows."""
     need_gpu()
     k = 256
-    n = 4096 if swiglu else 2048        # 16 or 8 N-tiles: >= 16 units per CTA on 152 SMs
-    if layout == "contiguous":
-        counts = streamed_counts(7 + swiglu, 9 if swiglu else 10, 2000 if swiglu else 3900, 60)
-    else:
-        counts = streamed_counts(9 + swiglu, 12 if swiglu else 34, 900, 60)
+    counts = streamed_counts(7 + swiglu + 2 * (layout == "batched") + n, n_big, big_rows, 60)
     counts.append(20)                   # the extra segment, short: streamed from w_extra
     num_w = len(counts) - 1
     S = len(counts)

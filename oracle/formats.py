@@ -10,8 +10,15 @@ no infinities.  Exponent field 0 holds subnormals m * 2^-9; exponent field 15 wi
 mantissa 7 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.  Encoding rounds
 to nearest, ties to even, and saturates finite values beyond 448 to +-448 ("satfinite").
 
+E2M1 (the element format of NVFP4, the 4-bit combine and dispatch units the Mega-MoE page
+names next to the FP8 ones): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no
+infinities or NaN.  Exponent field 0 holds the subnormal 0.5 * m, so the magnitudes are
+0, 0.5, 1, 1.5, 2, 3, 4 and 6.  Encoding rounds to nearest, ties to even, and saturates
+beyond 6.
+
 Pinned in tests/test_oracle_formats.py against torch's CPU casts (library routines) on
-exhaustive or large seeded sets, and against the definition's special cases.
+exhaustive or large seeded sets, and against the definition's special cases; E2M1 in
+tests/test_oracle_nvfp4.py against its value table and a brute-force nearest search.
 """
 import numpy as np
 
@@ -100,6 +107,44 @@ def e4m3_encode(x):
 def e4m3_round(x):
     """float32 -> nearest-even, saturated E4M3 value, returned as float32."""
     return e4m3_decode(e4m3_encode(x))
+
+
+E2M1_MAX = 6.0
+
+
+def e2m1_decode(codes):
+    """uint8 E2M1 codes (low 4 bits) -> float32 values (exact)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 0xF
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    ex = (c >> 1) & 0x3
+    man = c & 0x1
+    mag = np.where(ex == 0, 0.5 * man, (1.0 + 0.5 * man) * np.exp2(ex - 1.0))
+    return (sign * mag).astype(np.float32)
+
+
+def e2m1_encode(x):
+    """float32 array -> uint8 E2M1 codes: round to nearest even, saturate to +-6.
+
+    As for E4M3: in float64, the spacing of E2M1 values around |x| is 0.5 below 2 (the
+    subnormal step, which the first binade [1, 2) shares), else 2^(e-1) for
+    2^e <= |x| < 2^(e+1); |x| / spacing is rounded half to even and scaled back, clamped
+    to 6, and the code read off the rounded value.  NaN inputs are not defined for the
+    format and are not expected."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1
+    step = np.where(a < 2.0, 0.5, np.exp2(np.maximum(e, 1) - 1.0))
+    v = np.minimum(np.rint(a / step) * step, E2M1_MAX)
+    # codes: 0 0.5 1 1.5 2 3 4 6 -> 0..7
+    mag_code = np.where(v < 2.0, np.rint(v / 0.5), np.where(v < 4.0, 2 + v, 4 + v / 2.0)).astype(np.int64)
+    return (mag_code | np.where(neg, 0x8, 0)).astype(np.uint8)
+
+
+def e2m1_round(x):
+    """float32 -> nearest-even, saturated E2M1 value, returned as float32."""
+    return e2m1_decode(e2m1_encode(x))
 
 
 def round_up(x, y):

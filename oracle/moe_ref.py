@@ -11,7 +11,7 @@ MoonEP page (after dispatch the rows arrive grouped by expert).
 """
 import numpy as np
 
-from .formats import (bf16_bits_to_f32, e4m3_decode, e4m3_encode, f32_to_bf16_bits)
+from .formats import (bf16_bits_to_f32, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode, f32_to_bf16_bits)
 
 F32 = np.float32
 STATUS_BAD_EXPERT = 1
@@ -245,6 +245,42 @@ def qdq_f32(r, s):
     return (q / s).astype(F32)
 
 
+NVFP4_BLOCK = 16
+
+
+def nvfp4_qdq_f32(r, g):
+    """NVFP4 fake-quant of router-weighted rows (the Mega-MoE page runs its combine and
+    dispatch quantisers with NVFP4 units as well as FP8 ones, and leaves the format's
+    arithmetic to that recipe; this is the two-level NVFP4 reading).  r [..., H] float32,
+    H a multiple of 16; g the float32 per-tensor scale (448 * 6 / calibration amax).
+    For each block of 16 consecutive elements along the last axis, in float32:
+      a = max |r| over the block;
+      block scale code s_b = e4m3(fl32(fl32(a / 6) * g)) (nearest even, saturating);
+      inv = fl32(g / e4m3_decode(s_b)) (0 when s_b decodes to 0),
+      d   = fl32(e4m3_decode(s_b) / g);
+      each element: q = e2m1(fl32(r * inv)) (nearest even, saturating at 6),
+                    r' = fl32(e2m1_decode(q) * d).
+    Returns r' (float32, the shape of r)."""
+    r = np.asarray(r, dtype=F32)
+    g = F32(g)
+    blocks = r.reshape(r.shape[:-1] + (r.shape[-1] // NVFP4_BLOCK, NVFP4_BLOCK))
+    a = np.abs(blocks).max(axis=-1, keepdims=True).astype(F32)
+    sf = ((a / F32(6.0)).astype(F32) * g).astype(F32)
+    sdec = e4m3_decode(e4m3_encode(sf))
+    with np.errstate(divide="ignore"):
+        inv = np.where(sdec > 0, (g / np.where(sdec > 0, sdec, F32(1.0))).astype(F32), F32(0.0)).astype(F32)
+    d = (sdec / g).astype(F32)
+    q = e2m1_decode(e2m1_encode((blocks * inv).astype(F32)))
+    return (q * d).astype(F32).reshape(r.shape)
+
+
+def nvfp4_scale_from_amax(amax):
+    """Per-tensor NVFP4 scale 448 * 6 / amax in float32 (1 when amax is 0): the largest
+    block (amax / 6) maps onto the largest E4M3 block scale, 448."""
+    amax = F32(amax)
+    return F32(F32(2688.0) / amax) if amax > 0 else F32(1.0)
+
+
 # ------------------------------------------------------------------- dispatch fake-quant
 def dispatch_qdq_bits(x_bits, s):
     """Dispatch fake-quant of BF16 token rows (Mega-MoE page: the dispatch quantiser
@@ -262,7 +298,7 @@ def tensor_amax(x_bits):
 
 
 # --------------------------------------------------------------------------- combine
-def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale=None):
+def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale=None, fq_format="e4m3"):
     """Fixed-order combine (Mega-MoE page): per token, the valid slots in ascending
     order, each row router-weighted (float32 product of the BF16 row and the float32
     weight) and optionally fake-quantised, summed in float32 starting from +0, then the
@@ -275,6 +311,8 @@ def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale
     topk_w None: the rows are already router-weighted (the MoonEP page applies the route
     weights inside the expert computation, before the down projection's output is
     combined, so the combine only sums), and r = float(y).
+    fq_format: "e4m3" (qdq_f32 with the scale fq_scale) or "nvfp4" (nvfp4_qdq_f32 with the
+    per-tensor scale fq_scale).
     Returns out bits [T, H] uint16.
     """
     inv_map = np.asarray(inv_map)
@@ -291,7 +329,7 @@ def combine(y_bits, inv_map, topk_w, shared_bits=None, shared_map=None, fq_scale
         else:
             r = (y * np.asarray(topk_w, dtype=F32)[:, k:k + 1]).astype(F32)
         if fq_scale is not None:
-            r = qdq_f32(r, fq_scale)
+            r = nvfp4_qdq_f32(r, fq_scale) if fq_format == "nvfp4" else qdq_f32(r, fq_scale)
         acc = np.where(ok[:, None], (acc + r).astype(F32), acc)
     if shared_bits is not None:
         srow = np.arange(T) if shared_map is None else np.asarray(shared_map)
@@ -332,7 +370,7 @@ def _f64_weights(w_bits_or_f):
 
 
 def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
-                    fq_scale=None, fp8=False, dispatch_scale=None):
+                    fq_scale=None, fp8=False, dispatch_scale=None, fq_format="e4m3"):
     """Dense per-token reference MoE in fp64 (the MoonEP page validates its path by
     comparing with a straightforward per-token MoE): for each token, for the valid slots in ascending
     order, r = w_k * expert_{idx_k}(x_t) (optionally fake-quantised as in the combine);
@@ -347,6 +385,7 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     dispatch_scale: the routed experts see dispatch_qdq_bits(x, s) instead of x; the
     shared expert keeps the original x (the Mega-MoE page requires the shared expert to be
     unfused when the dispatch is quantised, since a fused one would read the same tokens).
+    fq_format: the combine fake-quant's format when fq_scale is given, "e4m3" or "nvfp4".
     Returns float64 [len(tokens), H].
     """
     x = bf16_bits_to_f32(np.asarray(x_bits)).astype(np.float64)
@@ -397,7 +436,8 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
         ok = sub_idx[:, k] >= 0
         r = wsub[:, k:k + 1].astype(np.float64) * contrib[:, k]
         if fq_scale is not None:
-            r = qdq_f32(r.astype(F32), fq_scale).astype(np.float64)
+            rq = nvfp4_qdq_f32 if fq_format == "nvfp4" else qdq_f32
+            r = rq(r.astype(F32), fq_scale).astype(np.float64)
         out = np.where(ok[:, None], out + r, out)
     if shared is not None:
         any_valid = (sub_idx >= 0).any(axis=1)

@@ -29,7 +29,7 @@ class MoeError(RuntimeError):
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
-                ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I)]
+                ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I), ("combine_fq_format", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -69,6 +69,8 @@ _SIGS = {
     "moe_combine_verify": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_combine_amax": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_fq_scale_from_amax": ([_P, _P, _P], _I),
+    "moe_combine_nvfp4": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_fq4_scale_from_amax": ([_P, _P, _P], _I),
     "moe_layer_workspace_bytes": ([ctypes.POINTER(LayerDesc)], _Z),
     "moe_layer_views": ([ctypes.POINTER(LayerDesc), _P, ctypes.POINTER(LayerViews)], _I),
     "moe_layer_forward": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeights), _P, _P, _P, _P, _P, _P, _P,
@@ -314,6 +316,20 @@ def moe_combine(y, inv_map, topk_w, shared_y=None, shared_map=None, fq_scale=Non
     return out
 
 
+def moe_combine_nvfp4(y, inv_map, topk_w, g_scale, shared_y=None, shared_map=None, out=None, stream=None):
+    """Combine with the NVFP4 fake-quant of every routed row (g_scale: the per-tensor
+    scale from moe_fq4_scale_from_amax)."""
+    _dev(y)
+    T, K = inv_map.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
+    _check("moe_combine_nvfp4", lib().moe_combine_nvfp4(_ptr(y), _ptr(inv_map), _ptr(topk_w), T, K, H,
+                                                        _ptr(shared_y), _ptr(shared_map), _ptr(g_scale), _ptr(out),
+                                                        _stream(stream)))
+    return out
+
+
 def moe_combine_verify(y, inv_map, topk_w, expected, dev_status, shared_y=None, shared_map=None, fq_scale=None,
                        stream=None):
     T, K = inv_map.shape
@@ -343,6 +359,13 @@ def moe_fq_scale_from_amax(amax, scale=None, stream=None):
     return scale
 
 
+def moe_fq4_scale_from_amax(amax, scale=None, stream=None):
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=amax.device)
+    _check("moe_fq4_scale_from_amax", lib().moe_fq4_scale_from_amax(_ptr(amax), _ptr(scale), _stream(stream)))
+    return scale
+
+
 class MoeLayer:
     """Holds a layer's descriptor, weight pointers and workspace; forward() is one
     moe_layer_forward call.  Weights: w13 [E, 2I, H], w2 [E, H, I] (+ shared [2I, H],
@@ -350,9 +373,11 @@ class MoeLayer:
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
-                 weight_in_down=False, max_tokens=0, fuse_combine=False):
+                 weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3"):
+        if combine_fq not in ("e4m3", "nvfp4"):
+            raise ValueError("combine_fq is 'e4m3' or 'nvfp4'")
         self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
-                              int(max_tokens), int(fuse_combine))
+                              int(max_tokens), int(fuse_combine), int(combine_fq == "nvfp4"))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

@@ -129,9 +129,120 @@ __global__ void __launch_bounds__(256) combine_kernel(
   }
 }
 
-__global__ void fq_scale_kernel(const float* amax, float* scale) {
+__global__ void fq_scale_kernel(const float* amax, float* scale, float top) {
   const float a = *amax;
-  *scale = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
+  *scale = a > 0.0f ? __fdiv_rn(top, a) : 1.0f;
+}
+
+// ------------------------------------------------------------------ NVFP4 fake-quant
+// The Mega-MoE page runs its combine quantiser with NVFP4 units as well as FP8 ones and
+// leaves the format's arithmetic to that recipe; this is the two-level NVFP4 reading.
+// Per 16 consecutive columns of a router-weighted row r (float32):
+//   a = max |r|;  s_b = e4m3(fl32(fl32(a / 6) * g)) with g the per-tensor scale;
+//   inv = fl32(g / s_b) (0 if s_b is 0);  d = fl32(s_b / g);
+//   r' = fl32(e2m1(fl32(r * inv)) * d),
+// e2m1 rounding to nearest even on the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 and saturating.
+
+// E2M1 round to nearest, ties to the even code, saturating at 6: the midpoints between
+// neighbouring magnitudes decide, and a midpoint goes to the neighbour whose code is even
+// (0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4).
+__device__ __forceinline__ float e2m1_round(float x) {
+  const float a = fabsf(x);
+  float m;
+  if (a <= 0.25f) m = 0.0f;
+  else if (a < 0.75f) m = 0.5f;
+  else if (a <= 1.25f) m = 1.0f;
+  else if (a < 1.75f) m = 1.5f;
+  else if (a <= 2.5f) m = 2.0f;
+  else if (a < 3.5f) m = 3.0f;
+  else if (a <= 5.0f) m = 4.0f;
+  else m = 6.0f;
+  return copysignf(m, x);
+}
+
+// One warp per (token, column part) as in combine_kernel; a 16-column block is the two
+// 8-column vectors of lanes 2m and 2m+1, which exchange their amax with one shuffle, so
+// every lane runs the same iterations (parts hold an even number of vectors).
+template <int KMAX, bool SPLIT>
+__global__ void __launch_bounds__(256) combine_nvfp4_kernel(
+    const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_map, const float* __restrict__ topk_w, int T,
+    int K, int H, const uint16_t* __restrict__ shared_y, const int32_t* __restrict__ shared_map,
+    const float* __restrict__ g_scale, uint16_t* __restrict__ out, int splits) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = H / 8;
+  const int per_part = SPLIT ? ((nvec + splits - 1) / splits + 1) & ~1 : nvec;
+  const float g = *g_scale;
+  const int n_items = SPLIT ? T * splits : T;
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < n_items; item += nw) {
+    const int t = SPLIT ? item / splits : item;
+    const int v_begin = SPLIT ? (item - t * splits) * per_part : 0;
+    const int v_end = SPLIT ? min(nvec, v_begin + per_part) : nvec;
+    if (v_begin >= v_end) continue;
+    int my_p = -1;
+    float my_w = 0.0f;
+    if (lane < K) {
+      my_p = inv_map[(size_t)t * K + lane];
+      my_w = topk_w ? topk_w[(size_t)t * K + lane] : 1.0f;
+    }
+    const unsigned valid = __ballot_sync(0xffffffffu, lane < K && my_p >= 0);
+    int srow = -1;
+    if (valid && shared_y) srow = shared_map ? shared_map[t] : t;
+    int p[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      p[j] = __shfl_sync(0xffffffffu, my_p, j);
+      w[j] = __shfl_sync(0xffffffffu, my_w, j);
+      if (j >= K) p[j] = -1;
+    }
+    for (int vb = v_begin; vb < v_end; vb += 32) {
+      const int v = vb + lane;
+      const bool act = v < v_end;     // the same for both lanes of a block (v_end is even)
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      uint4 ld[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        ld[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (p[j] >= 0 && act) ld[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)p[j] * H) + v);
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (p[j] < 0) continue;       // warp-uniform
+        const uint32_t u[4] = {ld[j].x, ld[j].y, ld[j].z, ld[j].w};
+        float r[8];
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float yv = __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16));
+          r[i] = __fmul_rn(yv, w[j]);
+          a = fmaxf(a, fabsf(r[i]));
+        }
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const float sdec = e4m3_to_f32(f32_to_e4m3(__fmul_rn(__fdiv_rn(a, 6.0f), g)));
+        const float inv = sdec > 0.0f ? __fdiv_rn(g, sdec) : 0.0f;
+        const float d = __fdiv_rn(sdec, g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e2m1_round(__fmul_rn(r[i], inv)), d));
+      }
+      if (!act) continue;
+      if (srow >= 0) {
+        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(shared_y + (size_t)srow * H) + v);
+        const uint32_t u[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          acc[i] = __fadd_rn(acc[i],
+                             __uint_as_float((i & 1) ? (u[i >> 1] & 0xffff0000u) : (u[i >> 1] << 16)));
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = (uint32_t)f32_to_bf16(acc[2 * i]) | ((uint32_t)f32_to_bf16(acc[2 * i + 1]) << 16);
+      reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 template <int MODE>
@@ -211,7 +322,42 @@ extern "C" moe_status_t moe_combine_amax(const uint16_t* y, const int32_t* inv_m
 extern "C" moe_status_t moe_fq_scale_from_amax(const float* amax, float* scale, void* stream) {
   using namespace moe;
   if (!amax || !scale) return MOE_ERR_ARG;
-  fq_scale_kernel<<<1, 1, 0, as_stream(stream)>>>(amax, scale);
+  fq_scale_kernel<<<1, 1, 0, as_stream(stream)>>>(amax, scale, 448.0f);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_fq4_scale_from_amax(const float* amax, float* scale, void* stream) {
+  using namespace moe;
+  if (!amax || !scale) return MOE_ERR_ARG;
+  fq_scale_kernel<<<1, 1, 0, as_stream(stream)>>>(amax, scale, 2688.0f);   // 448 * 6
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_combine_nvfp4(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T,
+                                          int K, int H, const uint16_t* shared_y, const int32_t* shared_map,
+                                          const float* g_scale, uint16_t* out, void* stream) {
+  using namespace moe;
+  moe_status_t st = check_combine_args(y, inv_map, topk_w, T, K, H, shared_y);
+  if (st != MOE_OK) return st;
+  if (!g_scale) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 15)) return MOE_ERR_ARG;
+  const int target_warps = num_sms() * 64;
+  const int splits = std::max(1, std::min(H / 8 / 32, target_warps / std::max(T, 1)));
+  const long long items = (long long)T * splits;
+  const int blocks = (int)std::min<long long>((items + 7) / 8, num_sms() * 16);
+  cudaStream_t s = as_stream(stream);
+#define MOE_NVFP4_LAUNCH(KM, SP)                                                                         \
+  combine_nvfp4_kernel<KM, SP><<<blocks, 256, 0, s>>>(y, inv_map, topk_w, T, K, H, shared_y, shared_map, \
+                                                      g_scale, out, splits)
+  if (splits > 1) {
+    if (K <= 8) MOE_NVFP4_LAUNCH(8, true); else MOE_NVFP4_LAUNCH(32, true);
+  } else {
+    if (K <= 8) MOE_NVFP4_LAUNCH(8, false); else MOE_NVFP4_LAUNCH(32, false);
+  }
+#undef MOE_NVFP4_LAUNCH
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

@@ -30,6 +30,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
       d->K > kMaxTopK || d->H % 128 || d->I % 128 || (d->has_shared != 0 && d->has_shared != 1) ||
       (d->weight_in_down != 0 && d->weight_in_down != 1) || d->max_tokens < 0 ||
       (d->fuse_combine != 0 && d->fuse_combine != 1) ||
+      (d->combine_fq_format != 0 && d->combine_fq_format != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -105,6 +106,8 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   const bool fp8 = d->dtype == MOE_E4M3;
   if (fp8 && (!w->w13_scales || !w->w2_scales)) return MOE_ERR_ARG;
   if (fp8 && dispatch_scale) return MOE_ERR_UNSUPPORTED;   // the FP8 path already quantises the dispatch
+  const bool fq4 = fq_scale && d->combine_fq_format == 1;
+  if (fq4 && d->fuse_combine) return MOE_ERR_UNSUPPORTED;
   if (d->has_shared && (!w->shared_w13 || !w->shared_w2 ||
                         (fp8 && (!w->shared_w13_scales || !w->shared_w2_scales))))
     return MOE_ERR_ARG;
@@ -142,6 +145,9 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                                   d->E, sx2, sx2s, d->dtype, MOE_EPI_NONE, v.y, nullptr, dev_status,
                                   wd ? v.row_weights : nullptr, stream);
     if (st != MOE_OK) return st;
+    if (fq4)
+      return moe_combine_nvfp4(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H,
+                               d->has_shared ? v.y : nullptr, v.shared_map, fq_scale, out, stream);
     return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
                        v.shared_map, fq_scale, out, stream);
   }
@@ -164,6 +170,9 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                            dev_status, wd ? v.row_weights : nullptr, stream);
   if (st != MOE_OK) return st;
   // with the router weights applied in the down projection the combine only sums
+  if (fq4)
+    return moe_combine_nvfp4(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H,
+                             d->has_shared ? v.y : nullptr, v.shared_map, fq_scale, out, stream);
   return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
                      v.shared_map, fq_scale, out, stream);
 }

@@ -57,7 +57,8 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
                                        rows; the slots past max_tokens were dropped */
 
 /* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
- * dispatch fake-quant options, 3 the batched expert layout). */
+ * dispatch fake-quant options, 3 the batched expert layout, 4 the NVFP4 combine
+ * fake-quant and moe_layer_desc_t.combine_fq_format). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -339,6 +340,27 @@ moe_status_t moe_combine_amax(const uint16_t* y, const int32_t* inv_map, const f
 /* scale = 448 / amax in float32 (1 if amax is 0), on the device. */
 moe_status_t moe_fq_scale_from_amax(const float* amax, float* scale, void* stream);
 
+/* Combine with NVFP4 fake-quant ([MegaMoE] runs its combine quantiser with NVFP4 units as
+ * well as FP8 ones; the page leaves the format's arithmetic to that recipe, and this is the
+ * two-level NVFP4 reading).  The same fixed-order sum as moe_combine, with every
+ * router-weighted routed row r fake-quantised per block of 16 consecutive columns, in
+ * float32 with IEEE roundings:
+ *     a = max |r| over the block
+ *     s_b = e4m3(fl32(fl32(a / 6) * g))          (nearest even, saturating; E4M3 block scale)
+ *     inv = fl32(g / s_b)  (0 if s_b is 0);  d = fl32(s_b / g)
+ *     r' = fl32(e2m1(fl32(r * inv)) * d)          (E2M1: 0, .5, 1, 1.5, 2, 3, 4, 6; nearest
+ *                                                  even, saturating at 6; sign kept)
+ * The shared slot is added last and unquantised.
+ *   g_scale    device float32: the per-tensor scale g (moe_fq4_scale_from_amax).
+ *   Other arguments and errors as moe_combine (H a multiple of 128, so of 16). */
+moe_status_t moe_combine_nvfp4(const uint16_t* y, const int32_t* inv_map, const float* topk_w, int T, int K,
+                               int H, const uint16_t* shared_y, const int32_t* shared_map,
+                               const float* g_scale, uint16_t* out, void* stream);
+/* NVFP4 per-tensor scale g = 448 * 6 / amax in float32 (1 if amax is 0), on the device:
+ * the largest block (amax / 6) maps onto the largest E4M3 block scale.  amax as from
+ * moe_combine_amax. */
+moe_status_t moe_fq4_scale_from_amax(const float* amax, float* scale, void* stream);
+
 /* ---------------------------------------------------------------------------- layer
  * The whole layer in one call, one stream, no host synchronisation:
  *   route (if logits) -> permute (+ FP8 quantisation for E4M3) -> grouped GEMM gate/up
@@ -356,6 +378,8 @@ typedef struct {
                          through moe_permute_batched / moe_grouped_gemm_batched (ABI 3) */
   int fuse_combine;   /* 1: the combine runs inside the down projection
                          (moe_grouped_gemm_combine); same output bit for bit (ABI 3) */
+  int combine_fq_format; /* with a combine fake-quant scale: 0 E4M3 (moe_combine), 1 NVFP4
+                            (moe_combine_nvfp4; not with fuse_combine) (ABI 4) */
 } moe_layer_desc_t;
 
 typedef struct {
@@ -394,11 +418,13 @@ moe_status_t moe_layer_views(const moe_layer_desc_t* d, void* ws, moe_layer_view
  *   logits     nullable float32 [T, E]: route inside the layer (num_tokens as in
  *              moe_route_topk) and write topk_idx / topk_w; NULL: topk_idx / topk_w are
  *              inputs (e.g. routed elsewhere, with padding slots set to -1 by the caller).
- *   x          BF16 [T, H];  fq_scale nullable device scalar (combine fake-quant);
+ *   x          BF16 [T, H];  fq_scale nullable device scalar (combine fake-quant: the
+ *              E4M3 scale, or the NVFP4 per-tensor scale when d->combine_fq_format is 1);
  *   dispatch_scale nullable device scalar (dispatch fake-quant, BF16 layers; see
  *              moe_permute_ex);
  *   out        BF16 [T, H];  ws / ws_bytes: workspace, 256-byte aligned.
- * Errors: as the step calls; MOE_ERR_WORKSPACE if ws_bytes < moe_layer_workspace_bytes. */
+ * Errors: as the step calls; MOE_ERR_WORKSPACE if ws_bytes < moe_layer_workspace_bytes;
+ * MOE_ERR_UNSUPPORTED for an NVFP4 combine fake-quant with fuse_combine. */
 moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_layer_weights_t* w,
                                const float* logits, const int32_t* num_tokens, int32_t* topk_idx,
                                float* topk_w, const uint16_t* x, const float* fq_scale,

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_host_only_calls(lib):
-    assert lib.moe_abi_version() == 3
+    assert lib.moe_abi_version() == 4
     assert lib.moe_status_string(2) == b"workspace too small"
     # scratch sized from the inputs: grows with T, K and E
     a = lib.moe_permute_workspace_bytes(128, 8, 256, 1)
@@ -73,6 +73,12 @@ def test_layer_workspace_size(lib):
     assert lib.moe_layer_views(ctypes.byref(df), 1 << 20, ctypes.byref(views)) == 0 and views.counters
     df.fuse_combine = 2
     assert lib.moe_layer_workspace_bytes(ctypes.byref(df)) == 0
+    # the combine fake-quant format is 0 (E4M3) or 1 (NVFP4); it does not change the workspace
+    n0 = lib.moe_layer_workspace_bytes(ctypes.byref(d0))
+    d0.combine_fq_format = 1
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(d0)) == n0 > 0
+    d0.combine_fq_format = 2
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(d0)) == 0
     db.max_tokens = -1
     assert lib.moe_layer_workspace_bytes(ctypes.byref(db)) == 0
     db.max_tokens = 1 << 24   # 257 blocks of 2^24 rows: more than 2^31 rows
@@ -87,6 +93,10 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.moe_grouped_gemm(None, None, None, 1, 16, 100, 256, None, None, 1, None, None, 0, 0, None, None,
                                 None, None) == 1
     assert lib.moe_combine(None, None, None, 4, 2, 100, None, None, None, None, None) == 1
+    # NVFP4 combine: H not a multiple of 128, or no per-tensor scale
+    assert lib.moe_combine_nvfp4(None, None, None, 4, 2, 100, None, None, None, None, None) == 1
+    assert lib.moe_combine_nvfp4(1 << 20, 1 << 20, None, 4, 2, 128, None, None, None, 1 << 20, None) == 1
+    assert lib.moe_fq4_scale_from_amax(None, None, None) == 1
     # batched layout: max_tokens < 1, or more than 2^31 rows
     assert lib.moe_permute_batched(None, 4, 2, 8, 0, 0, None, 128, 0, None, None, None, None, None, None, None, 0,
                                    None, None, None, None, None) == 1

@@ -153,11 +153,12 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
     layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine,
-                         weight_in_down=weight_in_down, **kw)
+                         weight_in_down=weight_in_down, combine_fq=w.fq_format, **kw)
     fq = None
     if w.fake_quant:
-        # combine fake-quant: the constant scale 448 / amax, amax calibrated (max) on a batch
-        # of 16 tokens drawn with seed + 1 through this layer's own weights (untimed)
+        # combine fake-quant: the constant scale 448 / amax (E4M3) or the per-tensor scale
+        # 448 * 6 / amax (NVFP4), amax calibrated (max) on a batch of 16 tokens drawn with
+        # seed + 1 through this layer's own weights (untimed)
         wc = synth.scaled(w, T=16, T_valid=16, fake_quant=False, graph=False)
         cal = moe.MoeLayer(wc.T, wc.H, wc.I, wc.E, wc.K, dtype, **kw)
         c_idx = torch.empty(wc.T, wc.K, dtype=torch.int32, device=device)
@@ -169,7 +170,7 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         cv = cal.views
         moe.moe_combine_amax(cal.view("y", (cv.cap, wc.H), torch.bfloat16),
                              cal.view("inv_map", (wc.T, wc.K), torch.int32), c_wt, amax)
-        fq = moe.moe_fq_scale_from_amax(amax)
+        fq = moe.moe_fq4_scale_from_amax(amax) if w.fq_format == "nvfp4" else moe.moe_fq_scale_from_amax(amax)
         torch.cuda.synchronize()
         del cal
     dq = None
@@ -278,8 +279,12 @@ def staged_step(st, w, events):
                                      d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
                                      wd_rows, s) == 0
     events[4].record()
-    assert L.moe_combine(v.y, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, d.H, v.y if d.has_shared else None,
-                         v.shared_map, p(st["fq"]), p(st["out"]), s) == 0
+    if st["fq"] is not None and d.combine_fq_format == 1:
+        assert L.moe_combine_nvfp4(v.y, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, d.H,
+                                   v.y if d.has_shared else None, v.shared_map, p(st["fq"]), p(st["out"]), s) == 0
+    else:
+        assert L.moe_combine(v.y, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, d.H,
+                             v.y if d.has_shared else None, v.shared_map, p(st["fq"]), p(st["out"]), s) == 0
     events[5].record()
 
 
@@ -509,8 +514,8 @@ def run_ours(args, rank, world, local_rank):
                    "layout": (f"batched [{w.E + int(w.shared)}, {max_tokens}, H] + masked_m" if max_tokens
                               else "contiguous expert-major rows + cu_seqlens"),
                    "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +
-                              (f", E4M3 fake-quant at the calibrated constant scale {float(st['fq'].item()):.5g}"
-                               if w.fake_quant else ""),
+                              (f", {'NVFP4' if w.fq_format == 'nvfp4' else 'E4M3'} fake-quant at the calibrated "
+                               f"constant scale {float(st['fq'].item()):.5g}" if w.fake_quant else ""),
                    "router_weight": ("applied in the down projection's epilogue (weighted rows; the combine sums)"
                                      if args.weight_in_down else "applied in the combine"),
                    "dispatch": (f"E4M3 fake-quant of the routed experts' rows at the per-tensor scale "

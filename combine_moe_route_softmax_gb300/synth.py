@@ -27,6 +27,8 @@ lm_eval / OLMoE runs need datasets and trained weights, which these stand in for
   hardware-counter profiles of the FP8 kernels.
 * ``prefill_fq`` the prefill workload with the combine's constant-scale FP8
   fake-quant; the scale comes from a calibration batch drawn with seed + 1.
+* ``prefill_fq4`` the same with the NVFP4 combine fake-quant (per-tensor scale 448*6/amax
+  from the same calibration batch).
 
 x ~ N(0, 1) in BF16.  Expert weights ~ N(0, std = 1/sqrt(fan_in)) in BF16 (fan_in = H for
 the gate/up rows, I for the down rows); W13 holds gate rows [0, I) then up rows [I, 2I).
@@ -52,6 +54,7 @@ class Workload:
     slot_pad: float   # probability that a slot is padding
     fake_quant: bool = False
     graph: bool = False
+    fq_format: str = "e4m3"   # the combine fake-quant's format: "e4m3" or "nvfp4"
 
 
 WORKLOADS = {
@@ -66,6 +69,8 @@ WORKLOADS = {
     "decode_small": Workload("decode_small", 128, 128, 7168, 2048, 64, 8, True, "e4m3", "uniform", 0.0),
     "prefill_fq": Workload("prefill_fq", 16384, 8192, 7168, 2048, 256, 8, True, "bf16", "zipf",
                            0.0, fake_quant=True, graph=True),
+    "prefill_fq4": Workload("prefill_fq4", 16384, 8192, 7168, 2048, 256, 8, True, "bf16", "zipf",
+                            0.0, fake_quant=True, graph=True, fq_format="nvfp4"),
 }
 
 

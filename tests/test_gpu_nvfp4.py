@@ -125,3 +125,26 @@ def test_nvfp4_combine_with_the_fused_combine_is_rejected():
     with pytest.raises(moe.MoeError) as e:
         layer.forward(x, out, idx, wt, logits=logits, fq_scale=torch.ones(1, device="cuda"))
     assert e.value.code == 3
+
+
+def test_combine_nvfp4_rounds_exact_ties_to_even_codes():
+    """Blocks whose scaled elements sit exactly on E2M1 midpoints (0.25, 0.75, ..., 5) and
+    beyond the largest value: each tie goes to the even code, as the oracle's E2M1."""
+    need_gpu()
+    T, K, H = 8, 2, 128
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0])
+    rows = np.zeros((T * K, H // 16, 16))
+    rows[:, :, 0] = 6.0                                     # block amax 6: scale 1 at g = 1
+    rows[:, :, 1:] = ties
+    rows = rows * np.exp2(np.arange(T * K) % 5 - 2)[:, None, None]
+    y = torch.from_numpy(f32_to_bf16_bits(rows.reshape(T * K, H).astype(np.float32)).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    inv = np.arange(T * K, dtype=np.int32).reshape(T, K)
+    w = np.ones((T, K), dtype=np.float32)
+    g = np.float32(1.0)
+    out = moe.moe_combine_nvfp4(y, torch.from_numpy(inv).cuda(), torch.from_numpy(w).cuda(),
+                                torch.tensor([g], device="cuda"))
+    want = ref.combine(bits(y), inv, w, fq_scale=g, fq_format="nvfp4")
+    assert np.array_equal(bits(out), want)
+    # and the ties did move: the fake-quantised sum differs from the plain one
+    assert not np.array_equal(want, ref.combine(bits(y), inv, w))

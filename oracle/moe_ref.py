@@ -282,13 +282,15 @@ def nvfp4_scale_from_amax(amax):
 
 
 # ------------------------------------------------------------------- dispatch fake-quant
-def dispatch_qdq_bits(x_bits, s):
+def dispatch_qdq_bits(x_bits, s, fmt="e4m3"):
     """Dispatch fake-quant of BF16 token rows (Mega-MoE page: the dispatch quantiser
     fake-quantises the tokens the experts receive, with a calibrated or constant global
-    scale).  In float32: t = x * s, snapped to E4M3 (nearest even, saturating), divided by
-    s, and rounded back to BF16 -- the experts' input type here.  Returns BF16 bits."""
+    scale).  E4M3: in float32, t = x * s, snapped to E4M3 (nearest even, saturating),
+    divided by s.  NVFP4 (fmt "nvfp4", the page's other unit): nvfp4_qdq_f32(x, s) with s
+    the per-tensor scale.  Either way rounded back to BF16 -- the experts' input type
+    here.  Returns BF16 bits."""
     x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16))
-    return f32_to_bf16_bits(qdq_f32(x, s))
+    return f32_to_bf16_bits(nvfp4_qdq_f32(x, s) if fmt == "nvfp4" else qdq_f32(x, s))
 
 
 def tensor_amax(x_bits):
@@ -370,7 +372,7 @@ def _f64_weights(w_bits_or_f):
 
 
 def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
-                    fq_scale=None, fp8=False, dispatch_scale=None, fq_format="e4m3"):
+                    fq_scale=None, fp8=False, dispatch_scale=None, fq_format="e4m3", dispatch_format="e4m3"):
     """Dense per-token reference MoE in fp64 (the MoonEP page validates its path by
     comparing with a straightforward per-token MoE): for each token, for the valid slots in ascending
     order, r = w_k * expert_{idx_k}(x_t) (optionally fake-quantised as in the combine);
@@ -385,7 +387,8 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     dispatch_scale: the routed experts see dispatch_qdq_bits(x, s) instead of x; the
     shared expert keeps the original x (the Mega-MoE page requires the shared expert to be
     unfused when the dispatch is quantised, since a fused one would read the same tokens).
-    fq_format: the combine fake-quant's format when fq_scale is given, "e4m3" or "nvfp4".
+    fq_format: the combine fake-quant's format when fq_scale is given, "e4m3" or "nvfp4";
+    dispatch_format: the dispatch fake-quant's, likewise.
     Returns float64 [len(tokens), H].
     """
     x = bf16_bits_to_f32(np.asarray(x_bits)).astype(np.float64)
@@ -421,7 +424,7 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     xs = prep_x(x[toks])
     xs_shared = xs
     if dispatch_scale is not None:
-        xq = dispatch_qdq_bits(np.asarray(x_bits)[toks], dispatch_scale)
+        xq = dispatch_qdq_bits(np.asarray(x_bits)[toks], dispatch_scale, dispatch_format)
         xs = prep_x(bf16_bits_to_f32(xq).astype(np.float64))
     # expert outputs for every (token, slot) pair of the subset, one expert at a time
     contrib = np.zeros((len(toks), K, H), dtype=np.float64)

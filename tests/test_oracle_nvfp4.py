@@ -111,3 +111,20 @@ def test_combine_with_nvfp4_on_grid_rows_equals_the_plain_combine():
     assert np.array_equal(ref.combine(yb, inv, w, fq_scale=g, fq_format="nvfp4"), ref.combine(yb, inv, w))
     yo = f32_to_bf16_bits((y * F32(1.1)).astype(F32))
     assert not np.array_equal(ref.combine(yo, inv, w, fq_scale=g, fq_format="nvfp4"), ref.combine(yo, inv, w))
+
+
+def test_nvfp4_dispatch_fake_quant_of_bf16_rows():
+    """Dispatch (the page's other NVFP4 unit): on-grid BF16 rows come back unchanged at
+    g = 1; off-grid rows land on the block grids and are rounded to BF16; the E4M3 default
+    is untouched by the format argument."""
+    from oracle.formats import bf16_bits_to_f32, f32_to_bf16_bits
+    rng = np.random.default_rng(6)
+    r = on_grid_rows(rng, 4, 8, [0, 2, -3, 1, 4, -1, 0, 3])
+    rb = f32_to_bf16_bits(r)
+    assert np.array_equal(ref.dispatch_qdq_bits(rb, F32(1.0), "nvfp4"), rb)
+    x = f32_to_bf16_bits((rng.standard_normal((4, 128)) * 2).astype(F32))
+    g = ref.nvfp4_scale_from_amax(ref.tensor_amax(x))
+    got = ref.dispatch_qdq_bits(x, g, "nvfp4")
+    assert np.array_equal(got, f32_to_bf16_bits(ref.nvfp4_qdq_f32(bf16_bits_to_f32(x), g)))
+    assert not np.array_equal(got, x)
+    assert np.array_equal(ref.dispatch_qdq_bits(x, F32(7.0)), ref.dispatch_qdq_bits(x, F32(7.0), "e4m3"))

@@ -135,7 +135,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=False, weight_in_down=False):
+def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=None, weight_in_down=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -153,7 +153,8 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         del w13, w2, s13, s2
         dtype = moe.MOE_E4M3
     layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine,
-                         weight_in_down=weight_in_down, combine_fq=w.fq_format, **kw)
+                         weight_in_down=weight_in_down, combine_fq=w.fq_format, dispatch_fq=dispatch_fq or "e4m3",
+                         **kw)
     fq = None
     if w.fake_quant:
         # combine fake-quant: the constant scale 448 / amax (E4M3) or the per-tensor scale
@@ -175,13 +176,13 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         del cal
     dq = None
     if dispatch_fq:
-        # dispatch fake-quant: the per-tensor scale 448 / max|x| over the batch's real tokens
-        # (untimed, as a calibration would be)
+        # dispatch fake-quant: the per-tensor scale 448 / max|x| (E4M3) or 448 * 6 / max|x|
+        # (NVFP4) over the batch's real tokens (untimed, as a calibration would be)
         if w.dtype != "bf16":
             raise SystemExit("--dispatch-fq applies to BF16 workloads (E4M3 rows are quantised anyway)")
         amax = torch.zeros(1, dtype=torch.float32, device=device)
         moe.moe_amax_bf16(x[:w.T_valid], amax)
-        dq = moe.moe_fq_scale_from_amax(amax)
+        dq = moe.moe_fq4_scale_from_amax(amax) if dispatch_fq == "nvfp4" else moe.moe_fq_scale_from_amax(amax)
         torch.cuda.synchronize()
     # slot padding of the workload (a fixed seeded mask), applied by the harness after routing
     pad = synth.slot_padding(w, seed, device=device) if w.slot_pad > 0 else None
@@ -241,11 +242,13 @@ def staged_step(st, w, events):
     if mt:
         assert L.moe_permute_batched(p(st["idx"]), d.T, d.K, d.E, d.has_shared, mt, p(st["x"]), d.H, d.dtype, v.xp,
                                      v.xp_scales, v.masked_m, v.src_row, v.inv_map, v.shared_map, p(scratch),
-                                     scratch_bytes, p(st["status"]), p(st["dq"]), wd_w, wd_rows, s) == 0
+                                     scratch_bytes, p(st["status"]), p(st["dq"]), d.dispatch_fq_format, wd_w,
+                                     wd_rows, s) == 0
     elif st["dq"] is not None or wd:
         assert L.moe_permute_ex(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
                                 v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
-                                scratch_bytes, p(st["status"]), p(st["dq"]), wd_w, wd_rows, s) == 0
+                                scratch_bytes, p(st["status"]), p(st["dq"]), d.dispatch_fq_format, wd_w, wd_rows,
+                                s) == 0
     else:
         assert L.moe_permute(p(st["idx"]), d.T, d.K, d.E, d.has_shared, p(st["x"]), d.H, d.dtype, v.xp,
                              v.xp_scales, v.cu_seqlens, v.src_row, v.inv_map, v.shared_map, p(scratch),
@@ -518,9 +521,10 @@ def run_ours(args, rank, world, local_rank):
                                f"constant scale {float(st['fq'].item()):.5g}" if w.fake_quant else ""),
                    "router_weight": ("applied in the down projection's epilogue (weighted rows; the combine sums)"
                                      if args.weight_in_down else "applied in the combine"),
-                   "dispatch": (f"E4M3 fake-quant of the routed experts' rows at the per-tensor scale "
-                                f"{float(st['dq'].item()):.5g} (448 / max|x|)" if st["dq"] is not None
-                                else "rows as they are"),
+                   "dispatch": (f"{'NVFP4' if args.dispatch_fq == 'nvfp4' else 'E4M3'} fake-quant of the "
+                                f"routed experts' rows at the per-tensor scale {float(st['dq'].item()):.5g} "
+                                f"({'448 * 6' if args.dispatch_fq == 'nvfp4' else '448'} / max|x|)"
+                                if st["dq"] is not None else "rows as they are"),
                    "l2": "no flush: every step streams the weights (far larger than L2) from HBM"},
         "gpu_launches": (sum(KERNELS_PER_STEP.values()) - int(args.fuse_combine)) * args.steps,
         "kernels": kernels,
@@ -558,10 +562,11 @@ def oracle_sample(w, tokens, seed=0):
     return logits[toks], bits(x[:tokens]), w13, w2, shared
 
 
-def oracle_step(w, sample, per_call=None, dispatch_fq=False):
+def oracle_step(w, sample, per_call=None, dispatch_fq=None):
     """The oracle's layer on the sample: route, permute, fp64 experts and the sum (per-call
-    seconds accumulated into `per_call` when given).  dispatch_fq: the routed experts see
-    the sample's rows fake-quantised at the oracle's own per-tensor scale."""
+    seconds accumulated into `per_call` when given).  dispatch_fq (None, "e4m3" or "nvfp4"):
+    the routed experts see the sample's rows fake-quantised in that format at the oracle's
+    own per-tensor scale."""
     from oracle import moe_ref as ref
     logits, xb, w13, w2, shared = sample
     t0 = time.perf_counter()
@@ -569,8 +574,12 @@ def oracle_step(w, sample, per_call=None, dispatch_fq=False):
     t1 = time.perf_counter()
     ref.permute(idx, w.E, with_shared=w.shared)
     t2 = time.perf_counter()
-    dq = ref.fq_scale_from_amax(ref.tensor_amax(xb)) if dispatch_fq else None
-    out = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared, dispatch_scale=dq)
+    dq = None
+    if dispatch_fq:
+        a = ref.tensor_amax(xb)
+        dq = ref.nvfp4_scale_from_amax(a) if dispatch_fq == "nvfp4" else ref.fq_scale_from_amax(a)
+    out = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared, dispatch_scale=dq,
+                              dispatch_format=dispatch_fq or "e4m3")
     t3 = time.perf_counter()
     if per_call is not None:
         for k, v in (("route", t1 - t0), ("permute", t2 - t1), ("experts_and_sum", t3 - t2)):
@@ -578,7 +587,7 @@ def oracle_step(w, sample, per_call=None, dispatch_fq=False):
     return out
 
 
-def cpu_baseline(w, tokens=8, reps=1, dispatch_fq=False):
+def cpu_baseline(w, tokens=8, reps=1, dispatch_fq=None):
     sample = oracle_sample(w, tokens)
     per_call = {}
     t0 = time.perf_counter()
@@ -612,8 +621,9 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{w.name}: T={w.T_valid} tokens in a {w.T}-row bucket, H={w.H}, I={w.I}, E={w.E}, "
                                f"top-{w.K}, shared={int(w.shared)}, {w.dtype}",
                    "tokens_per_step": args.ref_tokens,
-                   "dispatch": ("E4M3 fake-quant of the routed experts' rows at the per-tensor scale 448 / max|x|"
-                                if args.dispatch_fq else "rows as they are")},
+                   "dispatch": (f"{'NVFP4' if args.dispatch_fq == 'nvfp4' else 'E4M3'} fake-quant of the routed "
+                                f"experts' rows at a per-tensor scale from max|x|" if args.dispatch_fq
+                                else "rows as they are")},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "kind": "oracle", "cores": os.cpu_count(),
                          "sample": f"{args.ref_tokens} tokens per step through the numpy oracle"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -635,8 +645,9 @@ def main():
                     help="expert-major rows with cu_seqlens, or the batched [E, max_tokens, H] layout")
     ap.add_argument("--weight-in-down", action="store_true",
                     help="apply the router weights in the down projection's epilogue (the combine only sums)")
-    ap.add_argument("--dispatch-fq", action="store_true",
-                    help="BF16 workloads: E4M3 fake-quant of the routed experts' input rows (per-tensor scale)")
+    ap.add_argument("--dispatch-fq", nargs="?", const="e4m3", default=None, choices=["e4m3", "nvfp4"],
+                    help="BF16 workloads: fake-quant of the routed experts' input rows, E4M3 (default) or NVFP4, "
+                         "at a per-tensor scale from the batch's amax")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="run the combine inside the down projection (moe_grouped_gemm_combine)")
     ap.add_argument("--max-tokens", type=int, default=0,

@@ -29,7 +29,8 @@ class MoeError(RuntimeError):
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
-                ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I), ("combine_fq_format", _I)]
+                ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I), ("combine_fq_format", _I),
+                ("dispatch_fq_format", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -52,10 +53,10 @@ _SIGS = {
     "moe_permute": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P], _I),
     "moe_permute_noalloc_max_scratch_bytes": ([], _Z),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
-    "moe_permute_ex": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _P, _P, _P], _I),
+    "moe_permute_ex": ([_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _I, _P, _P, _P], _I),
     "moe_permute_batched_workspace_bytes": ([_I, _I, _I, _I], _Z),
-    "moe_permute_batched": ([_P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _P, _P,
-                             _P], _I),
+    "moe_permute_batched": ([_P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P, _I, _P,
+                             _P, _P], _I),
     "moe_amax_bf16": ([_P, _Z, _P, _P], _I),
     "moe_quantize_act_fp8": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_quantize_weight_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
@@ -137,10 +138,18 @@ def moe_permute_workspace_bytes(T, K, E, with_shared):
     return lib().moe_permute_workspace_bytes(T, K, E, int(with_shared))
 
 
+def _fmt(name):
+    """Fake-quant format name -> the C code (0 E4M3, 1 NVFP4)."""
+    if name not in ("e4m3", "nvfp4"):
+        raise ValueError("fake-quant format is 'e4m3' or 'nvfp4'")
+    return int(name == "nvfp4")
+
+
 def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, dev_status=None, stream=None,
-                dispatch_scale=None, topk_w=None):
+                dispatch_scale=None, topk_w=None, dispatch_format="e4m3"):
     """Returns dict(xp, xp_scales, cu_seqlens, src_row, inv_map, shared_map, row_weights).
-    dispatch_scale / topk_w select moe_permute_ex (dispatch fake-quant / row weights)."""
+    dispatch_scale / topk_w select moe_permute_ex (dispatch fake-quant in dispatch_format
+    "e4m3" or "nvfp4" / row weights)."""
     _dev(topk_idx)
     _dev(x)
     T, K = topk_idx.shape
@@ -170,7 +179,7 @@ def moe_permute(topk_idx, E, x, with_shared=False, out_dtype=MOE_BF16, ws=None, 
         _check("moe_permute_ex", lib().moe_permute_ex(
             _ptr(topk_idx), T, K, E, int(with_shared), _ptr(x), H, out_dtype, _ptr(xp), _ptr(xps), _ptr(cu),
             _ptr(src), _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-            _ptr(dispatch_scale), _ptr(topk_w), _ptr(roww), _stream(stream)))
+            _ptr(dispatch_scale), _fmt(dispatch_format), _ptr(topk_w), _ptr(roww), _stream(stream)))
     return dict(xp=xp, xp_scales=xps, cu_seqlens=cu, src_row=src, inv_map=inv, shared_map=smap, row_weights=roww)
 
 
@@ -179,7 +188,7 @@ def moe_permute_batched_workspace_bytes(T, K, E, with_shared):
 
 
 def moe_permute_batched(topk_idx, E, x, max_tokens, with_shared=False, out_dtype=MOE_BF16, ws=None,
-                        dev_status=None, stream=None, dispatch_scale=None, topk_w=None):
+                        dev_status=None, stream=None, dispatch_scale=None, topk_w=None, dispatch_format="e4m3"):
     """Batched layout: returns dict(xb [nseg, max_tokens, H], xb_scales, masked_m [nseg], src_row
     [nseg * max_tokens], inv_map, shared_map, row_weights)."""
     _dev(topk_idx)
@@ -202,7 +211,7 @@ def moe_permute_batched(topk_idx, E, x, max_tokens, with_shared=False, out_dtype
     _check("moe_permute_batched", lib().moe_permute_batched(
         _ptr(topk_idx), T, K, E, int(with_shared), max_tokens, _ptr(x), H, out_dtype, _ptr(xb), _ptr(xbs), _ptr(mm),
         _ptr(src), _ptr(inv), _ptr(smap), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-        _ptr(dispatch_scale), _ptr(topk_w), _ptr(roww), _stream(stream)))
+        _ptr(dispatch_scale), _fmt(dispatch_format), _ptr(topk_w), _ptr(roww), _stream(stream)))
     return dict(xb=xb, xb_scales=xbs, masked_m=mm, src_row=src, inv_map=inv, shared_map=smap, row_weights=roww)
 
 
@@ -373,11 +382,9 @@ class MoeLayer:
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
-                 weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3"):
-        if combine_fq not in ("e4m3", "nvfp4"):
-            raise ValueError("combine_fq is 'e4m3' or 'nvfp4'")
+                 weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3", dispatch_fq="e4m3"):
         self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
-                              int(max_tokens), int(fuse_combine), int(combine_fq == "nvfp4"))
+                              int(max_tokens), int(fuse_combine), _fmt(combine_fq), _fmt(dispatch_fq))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

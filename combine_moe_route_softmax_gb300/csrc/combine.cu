@@ -143,21 +143,6 @@ __global__ void fq_scale_kernel(const float* amax, float* scale, float top) {
 //   r' = fl32(e2m1(fl32(r * inv)) * d),
 // e2m1 rounding to nearest even on the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 and saturating.
 
-// E2M1 rounding of two elements with the hardware conversions: cvt.rn.satfinite.e2m1x2.f32
-// rounds to nearest, ties to the even code, and saturates at 6 (0.25 -> 0, 0.75 -> 1,
-// 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4, 7 -> 6), packing its first operand in
-// the high nibble; cvt.rn.f16x2.e2m1x2 decodes the pair exactly, high nibble to the high
-// half.  The GPU tests hold it to the oracle's E2M1, written from the format's definition,
-// bit for bit (and sign for sign).
-__device__ __forceinline__ void e2m1_round2(float lo, float hi, float& lo_q, float& hi_q) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.rn.f16x2.e2m1x2 %0, q;\n\t}"
-      : "=r"(h2)
-      : "f"(hi), "f"(lo));
-  lo_q = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
-  hi_q = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
-}
-
 // One warp per (token, column part) as in combine_kernel; a 16-column block is the two
 // 8-column vectors of lanes 2m and 2m+1, which exchange their amax with one shuffle, so
 // every lane runs the same iterations (parts hold an even number of vectors).

@@ -69,6 +69,21 @@ __device__ __forceinline__ float block_scale(float amax) {
   return s > 0.0f ? s : 1.0f;
 }
 
+// E2M1 rounding of two float32 values with the hardware conversions:
+// cvt.rn.satfinite.e2m1x2.f32 rounds to nearest, ties to the even code, and saturates at 6
+// (0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4, 7 -> 6), packing
+// its first operand in the high nibble; cvt.rn.f16x2.e2m1x2 decodes the pair exactly, high
+// nibble to the high half.  Held bit for bit (and sign for sign) to an E2M1 written from
+// the format's definition by the GPU tests.
+__device__ __forceinline__ void e2m1_round2(float lo, float hi, float& lo_q, float& hi_q) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.rn.f16x2.e2m1x2 %0, q;\n\t}"
+      : "=r"(h2)
+      : "f"(hi), "f"(lo));
+  lo_q = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+  hi_q = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -82,6 +97,7 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
                           moe_dtype_t out_dtype, void* xp, float* xp_scales, int32_t* cu_seqlens, int32_t* src_row,
                           int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
                           const float* dq_scale, const float* topk_w, float* row_w, int max_tokens,
-                          int32_t* masked_m, void* stream, int32_t* zero_buf, int zero_per_token);
+                          int32_t* masked_m, void* stream, int32_t* zero_buf, int zero_per_token,
+                          int dq_format = 0);
 
 }  // namespace moe

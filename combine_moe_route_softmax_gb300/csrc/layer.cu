@@ -31,6 +31,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
       (d->weight_in_down != 0 && d->weight_in_down != 1) || d->max_tokens < 0 ||
       (d->fuse_combine != 0 && d->fuse_combine != 1) ||
       (d->combine_fq_format != 0 && d->combine_fq_format != 1) ||
+      (d->dispatch_fq_format != 0 && d->dispatch_fq_format != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -130,7 +131,8 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
     st = permute_impl(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, nullptr,
                       v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch,
                       p.scratch_bytes, dev_status, dispatch_scale, wd ? topk_w : nullptr,
-                      wd ? v.row_weights : nullptr, mt, v.masked_m, stream, v.counters, d->H / 128);
+                      wd ? v.row_weights : nullptr, mt, v.masked_m, stream, v.counters, d->H / 128,
+                      d->dispatch_fq_format);
     if (st != MOE_OK) return st;
     st = moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, p.nseg, mt, d->H, 2 * d->I, w->w13,
                                   w->w13_scales, d->E, sx13, sx13s, d->dtype, MOE_EPI_SWIGLU, v.hs, v.hs_scales,
@@ -154,7 +156,7 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   st = permute_impl(topk_idx, d->T, d->K, d->E, d->has_shared, x, d->H, d->dtype, v.xp, v.xp_scales, v.cu_seqlens,
                     v.src_row, v.inv_map, v.shared_map, static_cast<uint8_t*>(ws) + p.off_scratch, p.scratch_bytes,
                     dev_status, dispatch_scale, wd ? topk_w : nullptr, wd ? v.row_weights : nullptr, 0, nullptr,
-                    stream, v.counters, d->H / 128);
+                    stream, v.counters, d->H / 128, d->dispatch_fq_format);
   if (st != MOE_OK) return st;
   st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
                         sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,

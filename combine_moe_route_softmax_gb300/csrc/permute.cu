@@ -282,12 +282,41 @@ __device__ __forceinline__ uint4 qdq8(const uint4 u, float s, const float* tbl) 
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Dispatch fake-quant of 8 BF16 values in NVFP4 (the page's other dispatch unit): the
+// 16-column block is these 8 and the 8 of the partner lane (lane ^ 1), whose amax arrives by
+// shuffle (every lane of the warp calls this), then as the combine's NVFP4 step --
+// s_b = e4m3(fl32(fl32(a / 6) * g)), q = e2m1(fl32(x * g / s_b)), fl32(q * s_b / g) -- with
+// g / s_b and s_b / g from per-code tables, and the result rounded to BF16.
+__device__ __forceinline__ uint4 qdq8_nvfp4(const uint4 u, float g, const float* inv_tbl, const float* d_tbl) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float v[8];
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    a = fmaxf(a, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  const uint8_t sc = f32_to_e4m3(__fmul_rn(__fdiv_rn(a, 6.0f), g));
+  const float inv = inv_tbl[sc], d = d_tbl[sc];
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float q0, q1;
+    e2m1_round2(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv), q0, q1);
+    o[i] = (uint32_t)f32_to_bf16(__fmul_rn(q0, d)) | ((uint32_t)f32_to_bf16(__fmul_rn(q1, d)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Source-ordered gather: one warp per token, the row read once in chunks of 4 16-byte
-// vectors per lane and written to each destination row.  With a dispatch scale (DQ), the
-// routed destinations get the fake-quantised row and the shared row the original.
+// vectors per lane and written to each destination row.  With a dispatch scale (DQ 1:
+// E4M3, 2: NVFP4), the routed destinations get the fake-quantised row and the shared row
+// the original.
 // With few tokens (decode) a token's columns are split over `splits` warps, each taking
 // a run of whole 128-vector groups, so that the GPU has enough warps in flight.
-template <bool DQ>
+template <int DQ>
 __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t* __restrict__ x, int T, int K,
                                                                   int H, const int32_t* __restrict__ inv_map,
                                                                   const int32_t* __restrict__ shared_map,
@@ -299,9 +328,19 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
   const int per_part = ((nvec + 127) / 128 + splits - 1) / splits * 128;   // vectors, whole groups
   const int ndst = K + 1;
   const float s = DQ ? *dq_scale : 1.0f;
-  __shared__ float dq_tbl[DQ ? 256 : 1];
-  if (DQ) {
+  __shared__ float dq_tbl[DQ == 1 ? 256 : 1];
+  __shared__ float inv_tbl[DQ == 2 ? 256 : 1], d_tbl[DQ == 2 ? 256 : 1];
+  if (DQ == 1) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) dq_tbl[i] = __fdiv_rn(e4m3_to_f32((uint8_t)i), s);
+    __syncthreads();
+  }
+  if (DQ == 2) {
+    // per block-scale code: g / decode(code) (0 for a zero scale) and decode(code) / g
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+      const float sd = e4m3_to_f32((uint8_t)i);
+      inv_tbl[i] = sd > 0.0f ? __fdiv_rn(s, sd) : 0.0f;
+      d_tbl[i] = __fdiv_rn(sd, s);
+    }
     __syncthreads();
   }
   for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * splits; item += nw) {
@@ -317,10 +356,14 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int v = v0 + lane + 32 * j;
+        r[j] = make_uint4(0u, 0u, 0u, 0u);
         if (v < v_end) {
           r[j] = __ldg(in + v);
-          if (DQ) q[j] = qdq8(r[j], s, dq_tbl);
+          if (DQ == 1) q[j] = qdq8(r[j], s, dq_tbl);
         }
+        // NVFP4: every lane takes part in the block's amax shuffle; a lane past v_end holds
+        // zeros, and so does its partner (parts hold whole 128-vector groups, v_end is even)
+        if (DQ == 2) q[j] = qdq8_nvfp4(r[j], s, inv_tbl, d_tbl);
       }
       unsigned m = live;
       while (m) {
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(256) permute_gather_bf16_kernel(const uint16_t
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int v = v0 + lane + 32 * j;
-          if (v < v_end) o[v] = (DQ && routed) ? q[j] : r[j];
+          if (v < v_end) o[v] = (DQ != 0 && routed) ? q[j] : r[j];
         }
       }
     }
@@ -581,7 +624,7 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
                           int32_t* src_row, int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
                           int32_t* dev_status, const float* dq_scale, const float* topk_w, float* row_w,
                           int max_tokens, int32_t* masked_m, void* stream, int32_t* zero_buf,
-                          int zero_per_token){
+                          int zero_per_token, int dq_format){
   if (T < 0 || K < 1 || K > kMaxTopK || E < 1 || E > kMaxExperts || H <= 0 || H % 128 != 0) return MOE_ERR_ARG;
   if (with_shared != 0 && with_shared != 1) return MOE_ERR_ARG;
   if (out_dtype != MOE_BF16 && out_dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -604,6 +647,7 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
   if (!topk_idx || !x || !xp || !src_row || !inv_map || (with_shared && !shared_map)) return MOE_ERR_ARG;
   if (out_dtype == MOE_E4M3 && !xp_scales) return MOE_ERR_ARG;
   if (dq_scale && out_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (dq_format != 0 && dq_format != 1) return MOE_ERR_ARG;
   if (row_w && !topk_w) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xp)) & 15) return MOE_ERR_ARG;
   if ((size_t)T * K + T > 0x7fffffffull) return MOE_ERR_ARG;
@@ -654,12 +698,15 @@ moe_status_t permute_impl(const int32_t* topk_idx, int T, int K, int E, int with
     permute_gather_bf16_bulk_kernel<<<blocks, bulk_warps * 32, smem, s>>>(x, T, K, H, inv_map, smap,
                                                                           static_cast<uint16_t*>(xp), dev_status);
   } else if (out_dtype == MOE_BF16)
-    if (dq_scale)
-      permute_gather_bf16_kernel<true><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
-                                                               static_cast<uint16_t*>(xp), splits);
+    if (dq_scale && dq_format == 1)
+      permute_gather_bf16_kernel<2><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
+                                                            static_cast<uint16_t*>(xp), splits);
+    else if (dq_scale)
+      permute_gather_bf16_kernel<1><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, dq_scale,
+                                                            static_cast<uint16_t*>(xp), splits);
     else
-      permute_gather_bf16_kernel<false><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, nullptr,
-                                                                static_cast<uint16_t*>(xp), splits);
+      permute_gather_bf16_kernel<0><<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, nullptr,
+                                                            static_cast<uint16_t*>(xp), splits);
   else
     permute_gather_e4m3_kernel<<<gblocks, 256, 0, s>>>(x, T, K, H, inv_map, smap, static_cast<uint8_t*>(xp),
                                                        xp_scales, splits);
@@ -682,11 +729,11 @@ extern "C" moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, in
                                        const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp,
                                        float* xp_scales, int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
                                        int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
-                                       const float* dispatch_scale, const float* topk_w, float* row_weights,
-                                       void* stream) {
+                                       const float* dispatch_scale, int dispatch_format, const float* topk_w,
+                                       float* row_weights, void* stream) {
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xp, xp_scales, cu_seqlens, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights, 0,
-                           nullptr, stream, nullptr, 0);
+                           nullptr, stream, nullptr, 0, dispatch_format);
 }
 
 extern "C" moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int K, int E, int with_shared,
@@ -694,11 +741,12 @@ extern "C" moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int 
                                             void* xb, float* xb_scales, int32_t* masked_m, int32_t* src_row,
                                             int32_t* inv_map, int32_t* shared_map, void* ws, size_t ws_bytes,
                                             int32_t* dev_status, const float* dispatch_scale,
-                                            const float* topk_w, float* row_weights, void* stream) {
+                                            int dispatch_format, const float* topk_w, float* row_weights,
+                                            void* stream) {
   if (max_tokens < 1) return MOE_ERR_ARG;
   return moe::permute_impl(topk_idx, T, K, E, with_shared, x, H, out_dtype, xb, xb_scales, nullptr, src_row,
                            inv_map, shared_map, ws, ws_bytes, dev_status, dispatch_scale, topk_w, row_weights,
-                           max_tokens, masked_m, stream, nullptr, 0);
+                           max_tokens, masked_m, stream, nullptr, 0, dispatch_format);
 }
 
 extern "C" moe_status_t moe_quantize_act_fp8(const uint16_t* x, int rows, int cols, uint8_t* q, float* scales,

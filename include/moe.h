@@ -58,7 +58,8 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 
 /* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
  * dispatch fake-quant options, 3 the batched expert layout, 4 the NVFP4 combine
- * fake-quant and moe_layer_desc_t.combine_fq_format). */
+ * and dispatch fake-quant (moe_combine_nvfp4, the dispatch_format arguments,
+ * moe_layer_desc_t.combine_fq_format / dispatch_fq_format). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -141,13 +142,16 @@ moe_status_t moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, i
                                  int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map,
                                  int32_t* shared_map, int32_t* dev_status, void* stream);
 
-/* moe_permute with two options (ABI 2):
+/* moe_permute with two options (ABI 2; dispatch_format ABI 4):
  *   dispatch_scale nullable device float32 s: dispatch fake-quant ([MegaMoE]: the dispatch
  *              quantiser fake-quantises the tokens the routed experts receive, with a
  *              calibrated or constant global scale; the shared expert must not see them,
- *              so the shared rows keep the original x).  Routed rows become
- *              bf16(float(e4m3_rn_satfinite(x * s)) / s), float32 steps.  BF16 output only
+ *              so the shared rows keep the original x).  BF16 output only
  *              (MOE_ERR_UNSUPPORTED for E4M3, whose rows are quantised anyway).
+ *   dispatch_format 0: E4M3 -- routed rows become bf16(float(e4m3_rn_satfinite(x * s)) / s),
+ *              float32 steps.  1: NVFP4 ([MegaMoE]'s other dispatch unit; s is the
+ *              per-tensor scale g = 448 * 6 / amax) -- per 16 consecutive columns the
+ *              moe_combine_nvfp4 step applied to x, rounded to BF16.  Else MOE_ERR_ARG.
  *   topk_w / row_weights  nullable; with both given, row_weights float32 [cap] receives each
  *              row's router weight (topk_w[t, k] of its slot, 1 for a shared row), for a down
  *              projection that applies the weights itself (moe_grouped_gemm_ex row_scale).
@@ -156,7 +160,7 @@ moe_status_t moe_permute_ex(const int32_t* topk_idx, int T, int K, int E, int wi
                             const uint16_t* x, int H, moe_dtype_t out_dtype, void* xp, float* xp_scales,
                             int32_t* cu_seqlens, int32_t* src_row, int32_t* inv_map, int32_t* shared_map,
                             void* ws, size_t ws_bytes, int32_t* dev_status, const float* dispatch_scale,
-                            const float* topk_w, float* row_weights, void* stream);
+                            int dispatch_format, const float* topk_w, float* row_weights, void* stream);
 
 /* Calibration of the dispatch scale: amax = max(amax, max |x|) over a BF16 tensor of n
  * elements (16-byte aligned).  amax is a device float32 the caller zeroes; then
@@ -240,15 +244,16 @@ moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int
  *   MOE_DEV_OVERFLOW is ORed into dev_status.  (With distinct experts per token a segment
  *   holds at most T rows, so max_tokens >= T never drops.)
  *   ws         at least moe_permute_batched_workspace_bytes(T, K, E, with_shared) bytes.
- *   dispatch_scale, topk_w, row_weights: as moe_permute_ex (row_weights [nseg*max_tokens]).
+ *   dispatch_scale, dispatch_format, topk_w, row_weights: as moe_permute_ex (row_weights
+ *              [nseg*max_tokens]).
  * Errors: as moe_permute_ex. */
 size_t moe_permute_batched_workspace_bytes(int T, int K, int E, int with_shared);
 moe_status_t moe_permute_batched(const int32_t* topk_idx, int T, int K, int E, int with_shared,
                                  int max_tokens, const uint16_t* x, int H, moe_dtype_t out_dtype, void* xb,
                                  float* xb_scales, int32_t* masked_m, int32_t* src_row, int32_t* inv_map,
                                  int32_t* shared_map, void* ws, size_t ws_bytes, int32_t* dev_status,
-                                 const float* dispatch_scale, const float* topk_w, float* row_weights,
-                                 void* stream);
+                                 const float* dispatch_scale, int dispatch_format, const float* topk_w,
+                                 float* row_weights, void* stream);
 
 /* moe_grouped_gemm_ex over the batched layout: segment s covers rows
  * [s*max_tokens, s*max_tokens + min(max(masked_m[s], 0), max_tokens)) of a, out,
@@ -380,6 +385,7 @@ typedef struct {
                          (moe_grouped_gemm_combine); same output bit for bit (ABI 3) */
   int combine_fq_format; /* with a combine fake-quant scale: 0 E4M3 (moe_combine), 1 NVFP4
                             (moe_combine_nvfp4; not with fuse_combine) (ABI 4) */
+  int dispatch_fq_format; /* with a dispatch fake-quant scale: 0 E4M3, 1 NVFP4 (ABI 4) */
 } moe_layer_desc_t;
 
 typedef struct {

@@ -99,7 +99,7 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.moe_fq4_scale_from_amax(None, None, None) == 1
     # batched layout: max_tokens < 1, or more than 2^31 rows
     assert lib.moe_permute_batched(None, 4, 2, 8, 0, 0, None, 128, 0, None, None, None, None, None, None, None, 0,
-                                   None, None, None, None, None) == 1
+                                   None, None, 0, None, None, None) == 1
     assert lib.moe_grouped_gemm_batched(None, None, None, 1, 0, 128, 256, None, None, 1, None, None, 0, 0, None,
                                         None, None, None, None) == 1
     assert lib.moe_grouped_gemm_batched(None, None, None, 1025, 1 << 22, 128, 256, None, None, 1025, None, None, 0,

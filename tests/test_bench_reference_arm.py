@@ -32,6 +32,12 @@ def test_reference_arm_follows_the_dispatch_fake_quant_option():
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
     assert d["config"]["dispatch"].startswith("E4M3 fake-quant") and d["value"] > 0
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "1", "--dispatch-fq", "nvfp4"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert d["config"]["dispatch"].startswith("NVFP4 fake-quant")
 
 
 def test_oracle_step_with_dispatch_fake_quant_changes_the_routed_input_only():
@@ -46,7 +52,7 @@ def test_oracle_step_with_dispatch_fake_quant_changes_the_routed_input_only():
     w = synth.WORKLOADS["tiny"]
     sample = bench.oracle_sample(w, 4)
     plain = bench.oracle_step(w, sample)
-    dq = bench.oracle_step(w, sample, None, True)
+    dq = bench.oracle_step(w, sample, None, "e4m3")
     logits, xb, w13, w2, shared = sample
     idx, wt = ref.route_topk(logits, w.K)
     want = ref.layer_reference(xb, idx, wt, w13, w2, shared=shared,

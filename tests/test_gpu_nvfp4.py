@@ -148,3 +148,75 @@ def test_combine_nvfp4_rounds_exact_ties_to_even_codes():
     assert np.array_equal(bits(out), want)
     # and the ties did move: the fake-quantised sum differs from the plain one
     assert not np.array_equal(want, ref.combine(bits(y), inv, w))
+
+
+@pytest.mark.parametrize("T,K,E,H,shared,layout", [
+    (300, 8, 64, 1024, True, "contiguous"),
+    (3, 8, 64, 7168, True, "contiguous"),      # few tokens: columns split over warps
+    (40, 4, 16, 1152, False, "contiguous"),    # 144 vectors: a ragged last group
+    (64, 4, 16, 512, True, "batched"),
+])
+def test_permute_nvfp4_dispatch_bit_exact(T, K, E, H, shared, layout):
+    """Routed rows get the NVFP4 fake-quant of x (BF16 result), shared rows the original."""
+    need_gpu()
+    rng = np.random.default_rng(T + H)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    g0 = torch.Generator("cuda").manual_seed(T)
+    x = (torch.randn(T, H, generator=g0, device="cuda") *
+         torch.exp(torch.randn(T, 1, generator=g0, device="cuda"))).to(torch.bfloat16)
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_amax_bf16(x, amax)
+    g = moe.moe_fq4_scale_from_amax(amax)
+    gs = host(g)[0]
+    assert gs == ref.nvfp4_scale_from_amax(ref.tensor_amax(bits(x)))
+    idx_d = torch.from_numpy(idx).cuda()
+    if layout == "contiguous":
+        res = moe.moe_permute(idx_d, E, x, with_shared=shared, dispatch_scale=g, dispatch_format="nvfp4")
+        rows_out = bits(res["xp"])
+        src = host(res["src_row"])
+    else:
+        res = moe.moe_permute_batched(idx_d, E, x, T, with_shared=shared, dispatch_scale=g, dispatch_format="nvfp4")
+        rows_out = bits(res["xb"]).reshape(-1, H)
+        src = host(res["src_row"])
+    xq = ref.dispatch_qdq_bits(bits(x), gs, "nvfp4")
+    xb = bits(x)
+    TK = T * K
+    for r, sidx in enumerate(src):
+        if sidx < 0:
+            continue
+        if sidx < TK:
+            assert np.array_equal(rows_out[r], xq[sidx // K]), r
+        else:
+            assert np.array_equal(rows_out[r], xb[sidx - TK]), r
+
+
+def test_layer_with_nvfp4_dispatch():
+    need_gpu()
+    w = scaled(WORKLOADS["prefill"], T=96, T_valid=72, H=512, I=256, E=16, K=4)
+    x = synth.hidden(w, 0, device="cuda")
+    logits = synth.router_logits(w, 0, device="cuda")
+    w13, w2, s13, s2 = synth.expert_weights(w, 0, device="cuda")
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_BF16, w13=w13, w2=w2, shared_w13=s13, shared_w2=s2,
+                         dispatch_fq="nvfp4")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_amax_bf16(x[:w.T_valid], amax)
+    g = moe.moe_fq4_scale_from_amax(amax)
+    idx = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(w.T, w.K, dtype=torch.float32, device="cuda")
+    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    n = torch.tensor([w.T_valid], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.forward(x, out, idx, wt, logits=logits, num_tokens=n, dispatch_scale=g, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    from gpu_helpers import ExpertBits
+    from oracle.formats import bf16_bits_to_f32
+    want = ref.layer_reference(bits(x), host(idx), host(wt), ExpertBits(w13), ExpertBits(w2),
+                               shared=(bits(s13), bits(s2)), tokens=np.arange(w.T_valid),
+                               dispatch_scale=host(g)[0], dispatch_format="nvfp4")
+    got = bf16_bits_to_f32(bits(out)).astype(np.float64)[:w.T_valid]
+    assert ref.max_rel_err(got, want) <= 2e-2
+    # the format matters: the E4M3 reading of the same scale gives another output
+    plain = ref.layer_reference(bits(x), host(idx), host(wt), ExpertBits(w13), ExpertBits(w2),
+                                shared=(bits(s13), bits(s2)), tokens=np.arange(w.T_valid))
+    assert ref.max_rel_err(got, plain) > 5e-3

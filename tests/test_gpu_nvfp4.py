@@ -220,3 +220,49 @@ def test_layer_with_nvfp4_dispatch():
     plain = ref.layer_reference(bits(x), host(idx), host(wt), ExpertBits(w13), ExpertBits(w2),
                                 shared=(bits(s13), bits(s2)), tokens=np.arange(w.T_valid))
     assert ref.max_rel_err(got, plain) > 5e-3
+
+
+def test_layer_with_every_option_together():
+    """NVFP4 dispatch and combine, router weights in the down projection and the batched
+    layout in one layer: the output is the oracle's NVFP4 re-sum of the layer's own
+    (weighted) expert rows, bit for bit, and the routed input rows are the oracle's NVFP4
+    dispatch of x."""
+    need_gpu()
+    w = scaled(WORKLOADS["prefill"], T=64, T_valid=48, H=512, I=256, E=8, K=4)
+    x = synth.hidden(w, 0, device="cuda")
+    logits = synth.router_logits(w, 0, device="cuda")
+    w13, w2, s13, s2 = synth.expert_weights(w, 0, device="cuda")
+    layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_BF16, w13=w13, w2=w2, shared_w13=s13, shared_w2=s2,
+                         weight_in_down=True, max_tokens=w.T, combine_fq="nvfp4", dispatch_fq="nvfp4")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_amax_bf16(x[:w.T_valid], amax)
+    gd = moe.moe_fq4_scale_from_amax(amax)
+    gc = torch.tensor([200.0], dtype=torch.float32, device="cuda")
+    idx = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(w.T, w.K, dtype=torch.float32, device="cuda")
+    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    n = torch.tensor([w.T_valid], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.forward(x, out, idx, wt, logits=logits, num_tokens=n, fq_scale=gc, dispatch_scale=gd, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    v, d = layer.views, layer.desc
+    y = layer.view("y", (v.cap, d.H), torch.bfloat16)
+    xp = layer.view("xp", (v.cap, d.H), torch.bfloat16)
+    inv = host(layer.view("inv_map", (d.T, d.K), torch.int32))
+    src = host(layer.view("src_row", (v.cap,), torch.int32))
+    smap = host(layer.view("shared_map", (d.T,), torch.int32))
+    yb = bits(y)
+    # rows are stored weighted: the combine only sums (topk_w None)
+    want = ref.combine(yb, inv, None, shared_bits=yb, shared_map=smap, fq_scale=np.float32(200.0), fq_format="nvfp4")
+    assert np.array_equal(bits(out), want)
+    xq = ref.dispatch_qdq_bits(bits(x), host(gd)[0], "nvfp4")
+    xpb = bits(xp)
+    TK = w.T * w.K
+    checked = 0
+    for r, s_ in enumerate(src):
+        if s_ < 0:
+            continue
+        assert np.array_equal(xpb[r], xq[s_ // w.K] if s_ < TK else bits(x)[s_ - TK]), r
+        checked += 1
+    assert checked == int((inv >= 0).sum()) + int((smap >= 0).sum())

@@ -146,8 +146,10 @@ __global__ void fq_scale_kernel(const float* amax, float* scale, float top) {
 // One warp per (token, column part) as in combine_kernel; a 16-column block is the two
 // 8-column vectors of lanes 2m and 2m+1, which exchange their amax with one shuffle, so
 // every lane runs the same iterations (parts hold an even number of vectors).
+// K <= 8 (KMAX 8): capped at 64 registers so that 4 blocks (32 warps) share an SM, as the
+// plain combine's; K > 8 keeps its 32-slot loads.
 template <int KMAX, bool SPLIT>
-__global__ void __launch_bounds__(256) combine_nvfp4_kernel(
+__global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 1) combine_nvfp4_kernel(
     const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_map, const float* __restrict__ topk_w, int T,
     int K, int H, const uint16_t* __restrict__ shared_y, const int32_t* __restrict__ shared_map,
     const float* __restrict__ g_scale, uint16_t* __restrict__ out, int splits) {

@@ -471,7 +471,7 @@ def run_ours(args, rank, world, local_rank):
         wk = work[name]
         if "flops" in wk:
             k["tflops"] = round(wk["flops"] / (stage_ms[name] * 1e-3) / 1e12, 1)
-            k["frac_tc"] = round(k["tflops"] / peaks["bf16_tflops_sustained"], 3)
+            k["frac_tc"] = round(k["tflops"] / peaks["bf16_tflops"], 3)
         gbs = wk["bytes"] / (stage_ms[name] * 1e-3) / 1e9
         k["gbs"] = round(gbs, 1)
         k["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
@@ -479,8 +479,10 @@ def run_ours(args, rank, world, local_rank):
     dom = max(("gemm_gate_up", "gemm_down"), key=lambda n: stage_ms[n])
     bound = "tensor" if w.dtype == "bf16" else "hbm"
     if bound == "tensor":
+        # each GEMM is timed per launch (a few milliseconds between CUDA events), so it is
+        # held against the burst tensor peak, not the seconds-long sustained one
         achieved = work[dom]["flops"] / (stage_ms[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = peaks["bf16_tflops"]
         unit = "TFLOP/s"
     else:
         achieved = work[dom]["bytes"] / (stage_ms[dom] * 1e-3) / 1e9
@@ -531,7 +533,7 @@ def run_ours(args, rank, world, local_rank):
         "rows": work["_rows"],
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 3), "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+                     "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
         "e2e": {"value": round(tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out[0].numel() * 2,

@@ -13,9 +13,6 @@
 // of a tile are 128 gate rows and the matching 128 up rows, so one MMA with N = 256
 // yields g and u for 128 output columns side by side in TMEM.
 //
-// CTA pairs (clusters of 2, when the N-tile count is even): the two CTAs hold two N-tiles
-// of one M-tile, each fetches half of the shared activation rows and multicasts them.
-//
 // Two roles.  The MMA pipeline below takes every segment when streaming is off, and the
 // segments of more than NS = 32 rows when it is on.  Streaming CTAs (the last ny CTAs of
 // the grid, BF16 and not fused, when the launch has at least 16 units per CTA) take the
@@ -198,35 +195,10 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
 }
-// Multicast variant: the box lands at the same shared-memory offset in every CTA of
-// cta_mask within the cluster and completes the transaction on each one's barrier there.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// Arrive (on MMA completion) on the barrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 template <bool FP8>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -323,7 +295,7 @@ __device__ __forceinline__ int seg_end(const int* bnd, int s, int max_tokens) {
 // N-tiles (one N-tile when the count is odd) every M-tile of the group in turn.  A round of
 // the grid then holds a few weight tiles read by many M-tiles, so a large expert's weights
 // cross HBM about once per group instead of once per round, while two consecutive units
-// still share an M-tile (CTA pairs multicast its rows).  mgroup = 0: M-tile-major order.
+// still share an M-tile (read from L2 by both).  mgroup = 0: M-tile-major order.
 // Used for the BF16 gate/up (7168-deep K: a weight tile is 3.7 MB); the down projection's
 // short units ran slower grouped (1.86 against 1.83 ms) and keep the M-tile-major order.
 constexpr int MGROUP_GATE_UP = 32;
@@ -435,11 +407,11 @@ __device__ __forceinline__ void zero_rowless_tokens(const Args& args, int w0, in
 }
 
 // ------------------------------------------------------------------------ kernel
-template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
+template <bool FP8, bool SWIGLU, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmBx, const __grid_constant__ CUtensorMap tmAh,
-                        const __grid_constant__ CUtensorMap tmAt, const Args args) {
+                        const __grid_constant__ CUtensorMap tmBx, const __grid_constant__ CUtensorMap tmAt,
+                        const Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -537,36 +509,33 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int total_units = prefix[nseg] * n_tiles;
   const int total_y = prefix_y[nseg] * n_tiles;
   // CTAs [gx, gridDim.x) stream; every CTA derives the same split from the same counts.
-  // Pairs stay whole (both counts even), so no cluster straddles the two roles.
   int ny = 0;
   if (total_y > 0) {
-    const int G = gridDim.x, step = PAIR ? 2 : 1;
+    const int G = gridDim.x;
     if (total_units == 0) {
       ny = G;
     } else {
       const float f = costs[1] / (costs[0] + costs[1]);
-      ny = step * static_cast<int>(f * static_cast<float>(G) / static_cast<float>(step) + 0.5f);
-      ny = min(max(ny, step), G - step);
+      ny = static_cast<int>(f * static_cast<float>(G) + 0.5f);
+      ny = min(max(ny, 1), G - 1);
     }
   }
   const int gx = static_cast<int>(gridDim.x) - ny;
   const bool y_role = static_cast<int>(blockIdx.x) >= gx;
-  // MMA-pipeline CTAs actually used: the fewest (in whole pairs) that keep the largest
-  // per-CTA unit count, so the last round of units is full instead of a few CTAs finishing
-  // alone (weight-streaming launches such as decode, where those few cannot draw the HBM
+  // MMA-pipeline CTAs actually used: the fewest that keep the largest per-CTA unit count,
+  // so the last round of units is full instead of a few CTAs finishing alone
+  // (weight-streaming launches such as decode, where those few cannot draw the HBM
   // bandwidth that all of them share); compute-bound launches keep their critical path.
   int gxu = gx;
   if (total_units > 0 && gx > 0) {
-    const int step = PAIR ? 2 : 1;
     const int per = (total_units + gx - 1) / gx;
-    gxu = min(gx, ((total_units + per - 1) / per + step - 1) / step * step);
+    gxu = min(gx, (total_units + per - 1) / per);
   }
   if (tid == 64) {
     const int nst = y_role ? YSTAGES : STAGES;
     for (int s = 0; s < nst; ++s) {
       mbar_init(bar_full(s), 1);
-      // PAIR (MMA pipeline): both CTAs' MMAs must release a stage
-      mbar_init(bar_empty(s), PAIR && !y_role ? 2 : 1);
+      mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -578,23 +547,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  // the peer's multicast copies and commits target this CTA's barriers: both CTAs of a
-  // pair initialise theirs before either issues anything
-  if (PAIR) cluster_sync_all();
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
   if (FUSE && total_units == 0) {
     // no rows at all: every token's output is +0
     zero_rowless_tokens(args, blockIdx.x * (THREADS / 32) + warp, gridDim.x * (THREADS / 32), lane);
-    if (PAIR) cluster_sync_all();
     return;
   }
-  // no work: nothing allocated yet (both CTAs of a pair leave together, after the closing
-  // cluster barrier that the teardown would otherwise hold)
+  // no work: nothing allocated yet
   if (y_role ? static_cast<int>(blockIdx.x) - gx >= total_y
-             : static_cast<int>(blockIdx.x) >= min(total_units, gxu)) {
-    if (PAIR) cluster_sync_all();
+             : static_cast<int>(blockIdx.x) >= min(total_units, gxu))
     return;
-  }
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -805,14 +766,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
           const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
-          if (PAIR) {
-            // the pair works on two n-tiles of the same m-tile: each CTA fetches half of the
-            // A rows once and multicasts it to both
-            tma_load_2d_mc(sa + crank * (A_BYTES / 2), &tmAh, kb * KE, w.row0 + (BM / 2) * crank, bar_full(stage),
-                           0x3);
-          } else {
-            tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
-          }
+          tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
           tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
           tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
           if (++stage == STAGES) {
@@ -859,10 +813,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t acc = (FP8 ? k : (kb | k)) != 0;
             tc_mma<FP8>(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, acc);
           }
-          if (PAIR)
-            tc_commit_mc(bar_empty(stage), 0x3);   // the stage is free only when both MMAs are done
-          else
-            tc_commit(bar_empty(stage));
+          tc_commit(bar_empty(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -1102,8 +1053,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
-  // neither CTA of a pair leaves while the other may still multicast into it
-  if (PAIR) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------------- host side
@@ -1135,39 +1084,18 @@ bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, bool SWIGLU, bool PAIR, bool FUSE>
-moe_status_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
-                        const CUtensorMap& at, const Args& args, int grid, size_t smem, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<FP8, SWIGLU, PAIR, FUSE>;
+template <bool FP8, bool SWIGLU, bool FUSE = false>
+moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& at,
+                    const Args& args, int grid, size_t smem, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<FP8, SWIGLU, FUSE>;
   static std::atomic<unsigned long long> attr_done{0};
   if (!once_per_device(attr_done, [&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) == cudaSuccess;
       }))
     return MOE_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = PAIR ? 2 : 1;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a, b, bx, ah, at, args) != cudaSuccess) return MOE_ERR_CUDA;
+  kern<<<grid, THREADS, smem, s>>>(a, b, bx, at, args);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
-}
-
-// CTA pairs (2-CTA clusters sharing A) when the unit count per m-tile is even, so the two
-// CTAs of a pair always hold two n-tiles of one m-tile.
-template <bool FP8, bool SWIGLU, bool FUSE = false>
-moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bx, const CUtensorMap& ah,
-                    const CUtensorMap& at, const Args& args, int grid, size_t smem, bool pair, cudaStream_t s) {
-  if (pair) return launch_one<FP8, SWIGLU, true, FUSE>(a, b, bx, ah, at, args, grid & ~1, smem, s);
-  return launch_one<FP8, SWIGLU, false, FUSE>(a, b, bx, ah, at, args, grid, smem, s);
 }
 
 }  // namespace gg
@@ -1221,9 +1149,8 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
        reinterpret_cast<uintptr_t>(out)) & 15)
     return MOE_ERR_ARG;
   if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
-  CUtensorMap ma, mb, mbx, mah, mat;
+  CUtensorMap ma, mb, mbx, mat;
   if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
-  if (!make_map(&mah, a, fp8, k_dim, rows_cap, BM / 2)) return MOE_ERR_CUDA;
   if (!make_map(&mat, a, fp8, k_dim, rows_cap, NS)) return MOE_ERR_CUDA;
   const void* wb = num_w > 0 ? w : w_extra;
   const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
@@ -1261,7 +1188,6 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
   const int grid = (int)std::min<long long>(num_sms(), max_units);
-  const bool pair = n_tiles % 2 == 0 && grid >= 2;
   // streaming CTAs for short segments: BF16, not fused, and a grid wide enough to split
   bool stream_on = !fp8 && !fuse && grid >= 16;
   int common_off = stream_on ? std::max(SmemLayout::x_end, SmemLayout::y_end) : SmemLayout::x_end;
@@ -1276,13 +1202,13 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   args.common_off = common_off;
   cudaStream_t s = as_stream(stream);
   if (fuse)
-    return fp8 ? launch<true, false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
-               : launch<false, false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
+    return fp8 ? launch<true, false, true>(ma, mb, mbx, mat, args, grid, smem, s)
+               : launch<false, false, true>(ma, mb, mbx, mat, args, grid, smem, s);
   if (fp8)
-    return swiglu ? launch<true, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
-                  : launch<true, false>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
-  return swiglu ? launch<false, true>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s)
-                : launch<false, false>(ma, mb, mbx, mah, mat, args, grid, smem, pair, s);
+    return swiglu ? launch<true, true>(ma, mb, mbx, mat, args, grid, smem, s)
+                  : launch<true, false>(ma, mb, mbx, mat, args, grid, smem, s);
+  return swiglu ? launch<false, true>(ma, mb, mbx, mat, args, grid, smem, s)
+                : launch<false, false>(ma, mb, mbx, mat, args, grid, smem, s);
 }
 }  // namespace gg
 }  // namespace moe

@@ -11,14 +11,19 @@
 //
 // The array's name in host code is only a host-side stand-in for the symbol, not a
 // device address: the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.  That set-up happens on the
-// first call on each device, so that first call should be made before any stream capture
-// begins.
+// cudaGetSymbolAddress (with that device current) and cached together with the CUDA
+// context it belongs to.  That set-up happens on the first call on each device, so that
+// first call should be made before any stream capture begins.  A device reset
+// (cudaDeviceReset) ends the context and may move the array; the next call sees a new
+// current context and looks the address up again, so it too belongs outside a capture.
 //
 // Every call on a device shares the one array.  Nothing in it has to start at zero: the
 // count kernel writes every entry the later kernels read.  Two calls whose kernels
 // overlap on the GPU (different streams without ordering between them) race on the
 // array and produce garbage; calls on one stream, or otherwise ordered, are safe.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -37,16 +42,37 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_permute_scratch on the current device (looked up once per device).
+// cuCtxGetCurrent from the CUDA driver, looked up once (the library links only the runtime).
+PFN_cuCtxGetCurrent_v4000 ctx_get_fn() {
+  static const PFN_cuCtxGetCurrent_v4000 fn = [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    return static_cast<PFN_cuCtxGetCurrent_v4000>(nullptr);
+  }();
+  return fn;
+}
+
+// Device address of g_permute_scratch on the current device: looked up once per device
+// and context (a device reset gives the device a new context, and the lookup is redone).
 moe_status_t static_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  const PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_get_fn();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  if (ctx == nullptr || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
+    // (the lookup also makes the device's primary context current when none is yet)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return MOE_ERR_CUDA;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return MOE_OK;

@@ -132,8 +132,10 @@ moe_status_t moe_permute(const int32_t* topk_idx, int T, int K, int E, int with_
  *   with MOE_ERR_WORKSPACE before anything is launched (e.g. E = 256 with a shared
  *   expert fits T up to about 65000 tokens; E = 1024 about 16000).
  * - The first call on each device looks up the array's device address (cudaGetSymbolAddress
- *   with that device current) and caches it; make that first call before any stream
- *   capture begins.  MOE_ERR_CUDA if the lookup fails.
+ *   with that device current) and caches it with the device's current context; make that
+ *   first call before any stream capture begins.  After a device reset the next call sees
+ *   a new context and looks the address up again (also outside a capture).  MOE_ERR_CUDA
+ *   if the lookup fails.
  * - All calls on a device share the array.  Nothing in it needs to start at zero, but calls
  *   whose kernels overlap on the GPU (unordered streams) race on it; order them. */
 size_t moe_permute_noalloc_max_scratch_bytes(void);

@@ -47,8 +47,8 @@ CASES = [
     ([0, 128, 256], 256, 128, 256, 2, False),
     ([0, 0, 1, 1], 8, 512, 512, 3, False),
     ([0, 2500, 5000], 5000, 512, 1024, 2, False),
-    # CTA pairs on two M-tiles of one weight tile (2, 4 and 4 M-tiles, the second of a pair
-    # holding 2 rows or 1 row) next to a one-row segment (a pair of N-tiles)
+    # ragged multi-tile segments (2, 4 and 4 M-tiles, the last holding 2 rows or 1 row) next
+    # to a one-row segment
     ([0, 130, 130, 515, 1000, 1001], 1100, 256, 512, 4, True),
 ]
 
@@ -149,11 +149,11 @@ def streamed_counts(seed, n_big, big_rows, n_small):
 
 STREAM_CASES = [
     # swiglu, layout, n (weight rows), big segments, their rows
-    (True, "contiguous", 4096, 9, 2000),      # 16 N-tiles: CTA pairs
+    (True, "contiguous", 4096, 9, 2000),      # 16 N-tiles
     (False, "contiguous", 2048, 10, 3900),    # 8 N-tiles
     (True, "batched", 4096, 12, 900),
     (False, "batched", 2048, 34, 900),
-    (True, "contiguous", 2816, 10, 2100),     # 11 N-tiles: no pairs, an odd streaming CTA count allowed
+    (True, "contiguous", 2816, 10, 2100),     # 11 N-tiles: an odd N-tile count
     (False, "contiguous", 2176, 10, 3000),    # 9 N-tiles, the last one half outside the weights
 ]
 
@@ -165,7 +165,7 @@ def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_row
     to streaming CTAs (weights as the MMA's M operand, the segment's rows as N = 32), the
     rest to the MMA pipeline.  Covers a short extra (shared-expert) segment, empty segments,
     row_scale on the plain epilogue, the batched layout's masked_m bounds, odd N-tile counts
-    (no CTA pairs) and a last N-tile that reaches past the weight rows."""
+    and a last N-tile that reaches past the weight rows."""
     need_gpu()
     k = 256
     counts = streamed_counts(7 + swiglu + 2 * (layout == "batched") + n, n_big, big_rows, 60)

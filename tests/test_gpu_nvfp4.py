@@ -49,7 +49,7 @@ def test_combine_nvfp4_bit_exact(T, K, E, H, pad, shared, weighted):
     g = moe.moe_fq4_scale_from_amax(amax)
     oa = ref.combine_amax(bits(y), inv, None if weighted else host(wt))
     assert host(amax)[0] == oa and host(g)[0] == ref.nvfp4_scale_from_amax(oa)
-    # a scale below the calibrated one as well: saturated block scales and elements
+    # a scale 4x above the calibrated one as well: saturated block scales and elements
     for gs in (host(g)[0], np.float32(host(g)[0] * 4)):
         gt = torch.tensor([gs], dtype=torch.float32, device="cuda")
         out = moe.moe_combine_nvfp4(y, invd, None if weighted else wt, gt, shared_y=y if shared else None,

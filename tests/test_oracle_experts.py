@@ -129,3 +129,94 @@ def test_layer_reference_dispatch_fake_quant_routes_quantised_tokens_only():
     shared_only = np.stack([brute_expert(f(xb)[t], f(shared[0]), f(shared[1])) for t in range(T)])
     assert np.allclose(ref, routed_only + shared_only, rtol=1e-12, atol=1e-12)
     assert not np.allclose(ref, layer_reference(xb, idx, w, w13, w2, shared=shared), rtol=1e-3, atol=0)
+
+
+# ------------------------------------------------------------------ FP8 branch, by loops
+def _e4m3_value(v):
+    """E4M3 rounding of one float32 value through torch's cast (a library routine, round
+    to nearest even), saturating at +-448 by the format's definition (e4m3fn has no inf)."""
+    import torch
+    v = max(-448.0, min(448.0, float(np.float32(v))))
+    return float(torch.tensor([v], dtype=torch.float32).to(torch.float8_e4m3fn).to(torch.float32).item())
+
+
+def _block_quant_loops(m, block_rows):
+    """Dequantised FP8 blocks of a float32 matrix, element by element: per block of
+    block_rows x 128, s = fl32(amax / 448) (1 for an all-zero block), each element
+    e4m3(fl32(v / s)) * s (the float32 division of the FP8 path, then fp64)."""
+    m = np.asarray(m, dtype=np.float32)
+    R, C = m.shape
+    out = np.zeros((R, C))
+    for r0 in range(0, R, block_rows):
+        for c0 in range(0, C, 128):
+            amax = 0.0
+            for r in range(r0, r0 + block_rows):
+                for c in range(c0, c0 + 128):
+                    amax = max(amax, abs(float(m[r, c])))
+            s = np.float32(np.float32(amax) / np.float32(448.0))
+            s = s if s > 0 else np.float32(1.0)
+            for r in range(r0, r0 + block_rows):
+                for c in range(c0, c0 + 128):
+                    out[r, c] = _e4m3_value(np.float32(m[r, c] / s)) * float(s)
+    return out
+
+
+def _fp8_expert_loops(x_row, w13, w2):
+    """One FP8 expert on one token, every step from its definition: x quantised per 1x128
+    block, W13 and W2 per 128x128 block, g and u as plain dot products, h = silu(g) * u
+    rounded to float32 and re-quantised per 1x128 block, then the down product."""
+    I = w13.shape[0] // 2
+    xq = _block_quant_loops(x_row[None, :], 1)[0]
+    w13q = _block_quant_loops(w13, 128)
+    w2q = _block_quant_loops(w2, 128)
+    h = np.zeros(I, dtype=np.float32)
+    for i in range(I):
+        g = math.fsum(w13q[i, c] * xq[c] for c in range(len(xq)))
+        u = math.fsum(w13q[I + i, c] * xq[c] for c in range(len(xq)))
+        h[i] = np.float32(g / (1.0 + math.exp(-g)) * u)
+    hq = _block_quant_loops(h[None, :], 1)[0]
+    return np.array([math.fsum(w2q[j, i] * hq[i] for i in range(I)) for j in range(w2.shape[0])]), h
+
+
+def test_fp8_layer_reference_matches_scalar_loops():
+    """The FP8 branch of the layer reference (x and h quantised per 1x128 block, weights per
+    128x128 block, the SwiGLU output re-quantised before the down projection) against
+    the same expert computed element by element, on routed slots and a shared expert with
+    H = I = 256 (two blocks along every axis).  A reference that skipped the re-quantisation
+    of h, or quantised h with one scale per 128 x 128 block, would differ by E4M3's rounding
+    error (percent level); the two checks at the end show this case tells them apart."""
+    rng = np.random.default_rng(6)
+    T, H, I, E, K = 3, 256, 256, 2, 2
+    xb = f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    idx, w = route_topk(rng.standard_normal((T, E)).astype(np.float32), K)
+    idx[2, 1] = -1
+    w13 = f32_to_bf16_bits((rng.standard_normal((E, 2 * I, H)) / 16).astype(np.float32))
+    w2 = f32_to_bf16_bits((rng.standard_normal((E, H, I)) / 16).astype(np.float32))
+    shared = (f32_to_bf16_bits((rng.standard_normal((2 * I, H)) / 16).astype(np.float32)),
+              f32_to_bf16_bits((rng.standard_normal((H, I)) / 16).astype(np.float32)))
+    ref8 = layer_reference(xb, idx, w, w13, w2, shared=shared, fp8=True)
+    f = lambda a: bf16_bits_to_f32(a)
+    x = f(xb)
+    want = np.zeros((T, H))
+    hs = []
+    for t in range(T):
+        for k in range(K):
+            if idx[t, k] < 0:
+                continue
+            y, h = _fp8_expert_loops(x[t], f(w13[idx[t, k]]), f(w2[idx[t, k]]))
+            want[t] += float(w[t, k]) * y
+            hs.append((h, f(w2[idx[t, k]])))
+        ys, _ = _fp8_expert_loops(x[t], f(shared[0]), f(shared[1]))
+        want[t] += ys
+    scale = np.abs(want).max()
+    assert np.allclose(ref8, want, rtol=1e-9, atol=1e-12 * scale)
+    # sensitivity: the down product of an un-requantised h, or of h quantised with a scale
+    # shared by the rows of a 128 x 128 block, moves the output far outside that bound
+    h, w2e = hs[0]
+    w2q = _block_quant_loops(w2e, 128)
+    per_row = w2q @ _block_quant_loops(h[None, :], 1)[0]
+    plain = w2q @ h.astype(np.float64)
+    h2 = np.stack([h, 3.7 * h])                      # a second row with a larger amax
+    shared_block = w2q @ _block_quant_loops(np.pad(h2, ((0, 126), (0, 0))), 128)[0]
+    assert np.abs(plain - per_row).max() > 1e-4 * np.abs(per_row).max()
+    assert np.abs(shared_block - per_row).max() > 1e-4 * np.abs(per_row).max()

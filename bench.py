@@ -15,9 +15,10 @@ Inputs are synthetic (seeded); the weights (22.6 GB) are far larger than L2, so 
 step streams them from HBM without an explicit flush.
 
 `--impl reference` times the CPU oracle (plain numpy, as it stands) on a bounded sample
-of the same workload on the host cores.  Under torchrun (N > 1) each rank runs an
-independent batch on its own GPU (token-sharded replicas, no collective in the data
-path); timing is the max over ranks.
+of the same workload on the host cores.  With --gpus N > 1 the script starts N ranks of
+one node itself (torch.distributed.run on 127.0.0.1) unless torchrun already did; each
+rank runs an independent batch on its own GPU (token-sharded replicas, no collective in
+the data path), timing is the max over ranks and rank 0 prints the line.
 """
 import argparse
 import json
@@ -68,6 +69,42 @@ def max_over_ranks(value, world, device="cpu"):
 def rank_seed(seed, rank):
     """Each rank draws its own batch (weak scaling); the weights are shared (same seed)."""
     return seed + 1000 * rank
+
+
+def max_stage_times(stage_ms, world, device="cpu"):
+    """Per-stage times of this rank -> the slowest rank's time of every stage."""
+    return {k: max_over_ranks(v, world, device) for k, v in stage_ms.items()}
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
+def emit(line, rank):
+    """The job's one JSON line, printed by rank 0 only; returns whether this rank printed."""
+    if rank != 0:
+        return False
+    print(json.dumps(line), flush=True)
+    return True
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(n, argv):
+    """`--gpus N` with N > 1 outside torchrun: run this script again as N ranks of one node
+    under torch.distributed.run (rendezvous on 127.0.0.1) and return their exit status;
+    None when this process is already a rank (or N == 1) and should do the work itself."""
+    if n <= 1 or "WORLD_SIZE" in os.environ:
+        return None
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
 
 
 # ---------------------------------------------------------------------- peaks/clocks
@@ -361,10 +398,8 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     # the call-by-call step is the layer's computation: same output bit for bit
     assert torch.equal(st["out"].view(torch.int16), layer_out.view(torch.int16)), "staged step differs from the layer"
-    stage_ms = {}
-    for j, name in enumerate(STAGES):
-        t = statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-        stage_ms[name] = max_over_ranks(t, world, device)
+    stage_ms = max_stage_times({name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                                for j, name in enumerate(STAGES)}, world, device)
 
     # --- the layer captured once into a CUDA graph: median of 20 warm replays (no host work
     # per step at all; the workspace and every buffer are fixed, so one capture serves)
@@ -464,7 +499,6 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
-    tok = w.T_valid * world
     kernels = {}
     for name in STAGES:
         k = {"ms": round(stage_ms[name], 4)}
@@ -498,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
            if world == 1 and not args.no_cpu_baseline else None)
     line = {
         "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
-        "value": round(tok / (ms * 1e-3), 1),
+        "value": round(whole_job_rate(w.T_valid, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -534,7 +568,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 3), "traffic": traffic,
                      "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
-        "e2e": {"value": round(tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(whole_job_rate(w.T_valid, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out[0].numel() * 2,
                 "pipeline": "inputs of step i+1 copied in and output of step i-1 copied out during step i; "
@@ -544,7 +578,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
-    print(json.dumps(line), flush=True)
+    emit(line, rank)
 
 
 # ------------------------------------------------------------------- CPU oracle arm
@@ -603,6 +637,7 @@ def cpu_baseline(w, tokens=8, reps=1, dispatch_fq=None):
 
 
 def run_reference(args, rank, world):
+    dist_init(world, "gloo")
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
@@ -630,7 +665,7 @@ def run_reference(args, rank, world):
                          "sample": f"{args.ref_tokens} tokens per step through the numpy oracle"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line, rank)
 
 
 def main():
@@ -658,12 +693,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    rc = launch_ranks(args.gpus, sys.argv[1:])
+    if rc is not None:
+        sys.exit(rc)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)
     if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.barrier()
         torch.distributed.destroy_process_group()
 
 

@@ -38,30 +38,13 @@
 // MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producer
 // waits (bounded) for its copies in flight, the MMA lane waits (bounded) for its MMAs,
 // and the TMEM is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace gg {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int KB_BYTES = 128;
 constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * KB_BYTES;
-constexpr int B_BYTES = BN * KB_BYTES;
-constexpr int B_HALF = B_BYTES / 2;
 constexpr int STAGE_TX = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + EPI_WARPS * 32;
-constexpr int TMEM_COLS = 512;
-constexpr int MAX_SEG = kMaxExperts + 1;
-constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
-
-constexpr int STAGE_OUT_PITCH = 80;                // 64 B of BF16 per row + 16 B pad (conflict-free)
-constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
 
 // Streamed segments (BF16, not fused): a segment of at most NS rows is computed by a
 // streaming CTA with the weights as the MMA's M operand (two M = 128 halves of a 256-row
@@ -69,7 +52,6 @@ constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
 // weight-sized stages.  Such a segment's units are bound by streaming their weights, and
 // one CTA keeps only four 32 KB weight tiles in flight behind 16 KB activation tiles that
 // hold a few real rows; here it keeps six behind 4 KB token tiles.
-constexpr int NS = 32;
 constexpr int YSTAGES = 6;
 constexpr int YT_BYTES = NS * KB_BYTES;
 constexpr int YSTAGE_BYTES = B_BYTES + YT_BYTES;   // 36 KB, a multiple of 1024
@@ -97,170 +79,6 @@ struct SmemLayout {
 };
 static_assert(SmemLayout::costs + 8 <= SmemLayout::arrays, "common tail header");
 static_assert(STAGES <= YSTAGES, "barrier slots");
-constexpr int SMEM_MAX = 227 * 1024;
-
-struct Args {
-  const int32_t* cu;        // cu_seqlens [nseg + 1], or masked_m [nseg] when max_tokens > 0
-  int max_tokens;           // 0: contiguous segments; > 0: segment s owns rows [s*max_tokens, ...)
-  int nseg;
-  int rows_cap;
-  int k_dim;
-  int n_dim;
-  int num_w;
-  const float* a_scales;
-  const float* w_scales;
-  const float* wx_scales;
-  void* out;
-  float* out_scales;
-  int32_t* dev_status;
-  const float* row_scale;   // plain epilogue: out row r is multiplied by row_scale[r] (nullable)
-  // fused combine (FUSE): out holds the BF16 expert rows; each token's output row is their
-  // fixed-order sum, computed by the warp whose store completes the token's 128-column block
-  const int32_t* src_row;   // row -> source index (t*K + k, or T*K + t for a shared row)
-  const int32_t* inv_map;   // [T, K] slot -> row or -1
-  const float* topk_w;      // [T, K] router weights, NULL for rows stored weighted
-  const int32_t* shared_map;  // [T] token -> shared row or -1 (nullable)
-  const float* fq_scale;    // combine fake-quant scale (nullable)
-  uint16_t* comb_out;       // [T, n_dim] BF16
-  int32_t* counters;        // [T, n_dim / 128], zero on entry, left zero
-  int T, K;
-  int stream;               // 1: segments of at most NS rows go to streaming CTAs
-  int common_off;           // shared-memory offset of the common tail
-};
-
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; false if the pipeline was aborted (by this wait timing out or another role).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > TIMEOUT_NS) {
-      *abort_flag = 1;
-      if (dev_status) atomicOr(dev_status, MOE_DEV_PIPELINE_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-// Bounded wait used while draining after an abort (ignores the abort flag).
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > TIMEOUT_NS) return;
-  }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-// With an L2 cache policy (createpolicy) attached to the copy.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-template <bool FP8>
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  if (FP8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-  }
-}
-// 32 consecutive float32 columns of this warp's 32 TMEM lanes (one row per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-// 16 consecutive float32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
-// 8-row groups 1024 bytes apart (stride byte offset), start address in 16-byte units.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused with 128B swizzle)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;             // descriptor version for tcgen05
-  d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
-  return d;
-}
-// Instruction descriptor: D float32, A/B K-major, N = BN, M = BM; A/B BF16 or E4M3.
-template <bool FP8>
-__host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
-}
-// BF16 x BF16 -> float32, M = 128 weight rows, N = NS token columns (streaming CTAs).
-__host__ __device__ constexpr uint32_t instr_desc_stream() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(NS >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
-}
-
 // Relative time of one unit (all units of a launch have the same K): an MMA-bound tile, a
 // single-tile segment's tile on the MMA pipeline, and a streamed unit.  They set how many
 // CTAs stream; measured per unit on the prefill expert mix with both roles running (gate/up:
@@ -274,65 +92,6 @@ constexpr int Y_EPI_WARPS = 4;
 // streaming CTAs' gigabytes do not push out the weight tiles that the MMA pipeline's
 // M-tiles of one segment share through L2.
 constexpr bool STREAM_EVICT_FIRST = true;
-
-// SiLU with the fast exponential and divide: their relative error (a few 1e-6) is far
-// below the BF16 or E4M3 rounding of h that follows; for g < -87 the denominator exceeds
-// 2^126 and the quotient flushes to 0, the limit of g * sigmoid(g).
-__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
-struct Unit {
-  int seg, row0, row_end, nt;
-};
-// Segment bounds kept in shared memory as bnd[]: contiguous segments [bnd[s], bnd[s+1]);
-// batched segments [s*max_tokens, bnd[s]) (bnd[s] = the segment's end row).
-__device__ __forceinline__ int seg_begin(const int* bnd, int s, int max_tokens) {
-  return max_tokens > 0 ? s * max_tokens : bnd[s];
-}
-__device__ __forceinline__ int seg_end(const int* bnd, int s, int max_tokens) {
-  return max_tokens > 0 ? bnd[s] : bnd[s + 1];
-}
-// Unit order within a segment: groups of `mgroup` M-tiles; inside a group, for each pair of
-// N-tiles (one N-tile when the count is odd) every M-tile of the group in turn.  A round of
-// the grid then holds a few weight tiles read by many M-tiles, so a large expert's weights
-// cross HBM about once per group instead of once per round, while two consecutive units
-// still share an M-tile (read from L2 by both).  mgroup = 0: M-tile-major order.
-// Used for the BF16 gate/up (7168-deep K: a weight tile is 3.7 MB); the down projection's
-// short units ran slower grouped (1.86 against 1.83 ms) and keep the M-tile-major order.
-constexpr int MGROUP_GATE_UP = 32;
-__device__ __forceinline__ Unit decode_unit(int u, int n_tiles, const int* cu, const int* prefix, int nseg,
-                                            int max_tokens, int mgroup) {
-  Unit w;
-  const int mt = u / n_tiles;
-  int lo = 0, hi = nseg - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= mt)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  w.seg = lo;
-  int lm;
-  if (mgroup == 0) {
-    lm = mt - prefix[lo];
-    w.nt = u - mt * n_tiles;
-  } else {
-    const int m = prefix[lo + 1] - prefix[lo];
-    const int l = u - prefix[lo] * n_tiles;
-    const int g = l / (mgroup * n_tiles);
-    const int gs = min(mgroup, m - g * mgroup);
-    const int r = l - g * mgroup * n_tiles;
-    const int npw = (n_tiles & 1) ? 1 : 2;
-    const int chunk = npw * gs;
-    const int np = r / chunk;
-    const int rr = r - np * chunk;
-    lm = g * mgroup + rr / npw;
-    w.nt = np * npw + (rr - (rr / npw) * npw);
-  }
-  w.row0 = seg_begin(cu, lo, max_tokens) + lm * BM;
-  w.row_end = seg_end(cu, lo, max_tokens);
-  return w;
-}
 
 // ----------------------------------------------------------------- fused combine
 // Columns [col, col + 128) of token t's output: the combine's arithmetic on the stored BF16
@@ -610,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int rA = SWIGLU ? wbase + nt * 128 : wbase + nt * BN;
             const int rB = SWIGLU ? wbase + args.n_dim / 2 + nt * 128 : rA + 128;
             for (int kb = 0; kb < kblocks; ++kb) {
-              if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status)) {
+              if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
                 ok = false;
                 break;
               }
@@ -646,13 +405,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int v = yi; ok && v < total_y; v += ny) {
             for (int kb = 0; kb < kblocks; ++kb) {
               if (kb == 0) {
-                if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status)) {
+                if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
               }
-              if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status)) {
+              if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
                 ok = false;
                 break;
               }
@@ -697,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           int seg, nt;
           y_unit(v, seg, nt);
           const int row0 = seg_begin(cu_s, seg, mtok), row_end = seg_end(cu_s, seg, mtok);
-          if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status)) break;
+          if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status, args.timeout_ns)) break;
           tc_fence_after();
           const uint32_t tb = tmem_base + lane_addr + buf * (2 * NS);
           uint32_t d0[NS], d1[NS];
@@ -757,7 +516,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rA = SWIGLU ? wbase + w.nt * 128 : wbase + w.nt * BN;
         const int rB = SWIGLU ? wbase + args.n_dim / 2 + w.nt * 128 : rA + 128;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status)) {
+          if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
             ok = false;
             break;
           }
@@ -794,13 +553,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           const bool round_start = FP8 || kb == 0;
           if (round_start) {
-            if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status)) {
+            if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
           }
-          if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status)) {
+          if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
             ok = false;
             break;
           }
@@ -880,7 +639,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       for (int rd = 0; rd < rounds; ++rd) {
-        if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status)) {
+        if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status, args.timeout_ns)) {
           ok = false;
           break;
         }
@@ -924,7 +683,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           tphase ^= 1;
         }
       }
-      if (!ok) break;
+      // FP8 SwiGLU: the eight warps exchange row maxima through a named barrier below, so
+      // they agree on leaving (one reduction per unit on every warp) before any of them does
+      if (FP8 && SWIGLU) {
+        if (bar_red_or(1, 32 * EPI_WARPS, !ok)) break;
+      } else if (!ok) {
+        break;
+      }
       // ---- tile epilogue from registers
       if (SWIGLU) {
         float h[64];
@@ -1070,8 +835,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// rows x inner-elements matrix, box = box_rows rows x 128 bytes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_t rows, uint32_t box_rows = 128) {
+bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint64_t esz = fp8 ? 1 : 2;
@@ -1122,7 +886,7 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
                               const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
                               moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
                               int32_t* dev_status, const float* row_scale, void* stream,
-                              const FuseIn* fuse = nullptr) {
+                              const FuseIn* fuse = nullptr, unsigned long long timeout_ns = TIMEOUT_NS) {
   const bool fp8 = dtype == MOE_E4M3;
   const bool swiglu = epilogue == MOE_EPI_SWIGLU;
   if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -1149,17 +913,6 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
        reinterpret_cast<uintptr_t>(out)) & 15)
     return MOE_ERR_ARG;
   if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
-  CUtensorMap ma, mb, mbx, mat;
-  if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
-  if (!make_map(&mat, a, fp8, k_dim, rows_cap, NS)) return MOE_ERR_CUDA;
-  const void* wb = num_w > 0 ? w : w_extra;
-  const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
-  if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
-  if (w_extra) {
-    if (!make_map(&mbx, w_extra, fp8, k_dim, n_dim)) return MOE_ERR_CUDA;
-  } else {
-    mbx = mb;
-  }
   Args args;
   args.cu = cu_seqlens;
   args.max_tokens = max_tokens;
@@ -1184,6 +937,25 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   args.counters = fuse ? fuse->counters : nullptr;
   args.T = fuse ? fuse->T : 0;
   args.K = fuse ? fuse->K : 1;
+  args.timeout_ns = timeout_ns;
+  cudaStream_t s = as_stream(stream);
+  // BF16 without the fused combine: CTA pairs with the 2-SM MMA (gemm2sm.cu)
+  if (!fp8 && !fuse) {
+    args.stream = 1;
+    args.common_off = 0;
+    return launch_2sm(a, rows_cap, k_dim, n_dim, w, num_w, w_extra, swiglu, args, true, s);
+  }
+  CUtensorMap ma, mb, mbx, mat;
+  if (!make_map(&ma, a, fp8, k_dim, rows_cap)) return MOE_ERR_CUDA;
+  if (!make_map(&mat, a, fp8, k_dim, rows_cap, NS)) return MOE_ERR_CUDA;
+  const void* wb = num_w > 0 ? w : w_extra;
+  const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
+  if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
+  if (w_extra) {
+    if (!make_map(&mbx, w_extra, fp8, k_dim, n_dim)) return MOE_ERR_CUDA;
+  } else {
+    mbx = mb;
+  }
   // grid: one CTA per SM, never more than the largest possible number of tiles
   const int n_tiles = swiglu ? (n_dim / 2) / 128 : (n_dim + BN - 1) / BN;
   const long long max_units = ((long long)(rows_cap + BM - 1) / BM + num_segments) * n_tiles;
@@ -1200,7 +972,6 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   if (smem > (size_t)SMEM_MAX) return MOE_ERR_ARG;
   args.stream = stream_on ? 1 : 0;
   args.common_off = common_off;
-  cudaStream_t s = as_stream(stream);
   if (fuse)
     return fp8 ? launch<true, false, true>(ma, mb, mbx, mat, args, grid, smem, s)
                : launch<false, false, true>(ma, mb, mbx, mat, args, grid, smem, s);
@@ -1221,6 +992,20 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
                                             const float* row_scale, void* stream) {
   return moe::gg::gemm_impl(a, a_scales, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
                             w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream);
+}
+
+// Test hook, deliberately absent from the public header: moe_grouped_gemm_ex with the limit
+// of each pipeline wait given in nanoseconds instead of the built-in 2 s, so that a test can
+// make a wait run out and check the abort path (MOE_DEV_PIPELINE_TIMEOUT set, the call
+// returns, the next call is unaffected) without faulting or hanging anything.
+extern "C" moe_status_t moe_testing_grouped_gemm_wait_limit(
+    const void* a, const float* a_scales, const int32_t* cu_seqlens, int num_segments, int rows_cap, int k_dim,
+    int n_dim, const void* w, const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
+    moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales, int32_t* dev_status,
+    const float* row_scale, unsigned long long wait_limit_ns, void* stream) {
+  return moe::gg::gemm_impl(a, a_scales, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
+                            w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream,
+                            nullptr, wait_limit_ns);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_combine(

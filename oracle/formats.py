@@ -56,9 +56,8 @@ def bf16_round(x):
     return bf16_bits_to_f32(f32_to_bf16_bits(x))
 
 
-def e4m3_decode(codes):
-    """uint8 E4M3 codes -> float32 values (exact); codes 0x7F / 0xFF decode to NaN."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _e4m3_value(c):
+    """Value of E4M3 codes (int64 array) from the format definition."""
     sign = np.where(c & 0x80, -1.0, 1.0)
     ex = (c >> 3) & 0xF
     man = c & 0x7
@@ -69,39 +68,39 @@ def e4m3_decode(codes):
     return (sign * mag).astype(np.float32)
 
 
+# the value of every one of the 256 codes, from the definition above
+_E4M3_TABLE = _e4m3_value(np.arange(256, dtype=np.int64))
+
+
+def e4m3_decode(codes):
+    """uint8 E4M3 codes -> float32 values (exact); codes 0x7F / 0xFF decode to NaN.
+    A lookup in the table of all 256 code values."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
 def e4m3_encode(x):
     """float32 array -> uint8 E4M3 codes: round to nearest even, saturate to +-448.
 
-    Works in float64, where every float32 input and every scaling by a power of two is
-    exact.  The spacing of E4M3 values around |x| is 2^-9 below the smallest normal
-    2^-6, else 2^(e-3) for 2^e <= |x| < 2^(e+1); |x| / spacing is rounded half to even
-    (np.rint) and scaled back.  A value that rounds past 448 is clamped to 448.  The
-    code is then read off the rounded value, so a rounding carry into the next binade
-    is handled by construction.
+    Read off the float32 bit pattern.  At or above the smallest normal 2^-6, E4M3 keeps 3
+    of float32's 23 fraction bits: the 20 dropped bits are rounded to nearest, ties to
+    even (adding 0x7FFFF plus the lowest kept bit, then shifting; a carry moves into the
+    exponent, which is the correctly rounded result), and the exponent is rebiased from
+    127 to 7, i.e. the code is the shifted pattern minus (127 - 7) << 3.  Below 2^-6 the
+    values are the multiples m * 2^-9 (m = 0..8, 8 being 2^-6 itself), so the code is
+    |x| * 2^9 rounded half to even.  Codes past 126 (448) saturate to 126; NaN gives
+    0x7F.  The sign bit is copied.
     """
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    neg = np.signbit(x)
-    a = np.abs(x)
-    nan = np.isnan(a)
-    a = np.where(nan, 0.0, a)
-    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
-    e = ex.astype(np.int64) - 1               # a in [2^e, 2^(e+1))
-    step = np.where(a < E4M3_MIN_NORMAL, E4M3_SUBNORMAL_STEP,
-                    np.exp2(np.maximum(e, -6) - 3.0))
-    v = np.rint(a / step) * step
-    v = np.minimum(v, E4M3_MAX)
-    # code from the (exactly representable) rounded magnitude v
-    _, vex = np.frexp(v)
-    ve = vex.astype(np.int64) - 1
-    is_sub = v < E4M3_MIN_NORMAL
-    sub_code = np.rint(v / E4M3_SUBNORMAL_STEP).astype(np.int64)
-    safe_e = np.where(is_sub, 0, ve)
-    man = np.rint((v / np.exp2(safe_e) - 1.0) * 8.0).astype(np.int64)
-    norm_code = ((safe_e + 7) << 3) | man
-    code = np.where(is_sub, sub_code, norm_code)
-    code = np.where(nan, 0x7F, code)
-    code = code | np.where(neg, 0x80, 0)
-    return code.astype(np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    mag = u & np.uint32(0x7FFFFFFF)
+    nan = mag > np.uint32(0x7F800000)
+    kept = (mag + np.uint32(0x7FFFF) + ((mag >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)
+    norm = kept.view(np.int32) - np.int32((127 - 7) << 3)
+    sub = np.rint(np.abs(x) * np.float32(512.0)).astype(np.int32)
+    code = np.where(mag < np.uint32(0x3C800000), sub, norm)     # 0x3C800000 = 2^-6
+    code = np.minimum(code, np.int32(0x7E))
+    code = np.where(nan, np.int32(0x7F), code)
+    return (code | ((u >> np.uint32(24)) & np.uint32(0x80)).view(np.int32)).astype(np.uint8)
 
 
 def e4m3_round(x):

@@ -211,9 +211,9 @@ def weight_quant_128x128(w):
 
 def dequant(codes, scales, block_rows):
     """codes * scale in float64, the scale block being block_rows x 128."""
-    v = e4m3_decode(codes).astype(np.float64)
-    s = np.repeat(np.repeat(scales.astype(np.float64), block_rows, axis=0), 128, axis=1)
-    return v * s
+    R, C = codes.shape
+    v = e4m3_decode(codes).astype(np.float64).reshape(R // block_rows, block_rows, C // 128, 128)
+    return (v * scales.astype(np.float64)[:, None, :, None]).reshape(R, C)
 
 
 # --------------------------------------------------------------------------- experts

@@ -81,3 +81,43 @@ def test_bf16_ties_and_overflow():
 @pytest.mark.parametrize("x,y,r", [(0, 128, 0), (1, 128, 128), (128, 128, 128), (129, 128, 256)])
 def test_round_up(x, y, r):
     assert round_up(x, y) == r
+
+
+def e4m3_encode_by_spacing(x):
+    """A second restatement of E4M3 rounding, by value rather than by bit pattern: in
+    float64 the spacing of E4M3 values around |x| is 2^-9 below 2^-6, else 2^(e-3) for
+    2^e <= |x| < 2^(e+1); |x| / spacing is rounded half to even and scaled back, clamped
+    to 448, and the code read off the rounded value."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, a)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.exp2(np.maximum(e, -6) - 3.0))
+    v = np.minimum(np.rint(a / step) * step, 448.0)
+    _, vex = np.frexp(v)
+    ve = vex.astype(np.int64) - 1
+    is_sub = v < 2.0 ** -6
+    safe_e = np.where(is_sub, 0, ve)
+    man = np.rint((v / np.exp2(safe_e) - 1.0) * 8.0).astype(np.int64)
+    code = np.where(is_sub, np.rint(v / 2.0 ** -9).astype(np.int64), ((safe_e + 7) << 3) | man)
+    code = np.where(nan, 0x7F, code) | np.where(neg, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def test_e4m3_encode_agrees_with_the_spacing_restatement():
+    """Bit-pattern rounding against value rounding: every float32 pattern in [2^-12, 512]
+    that lies within 64 ulp of an E4M3 value or of a halfway point between two of them
+    (the places where a rounding rule can go wrong), and 4 M random bit patterns."""
+    vals = e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    mids = (vals[1:] + vals[:-1]) / 2
+    pts = np.concatenate([vals[1:], mids, [464.0, 480.0, 512.0]]).astype(np.float32).view(np.uint32)
+    near = (pts[:, None].astype(np.int64) + np.arange(-64, 65)[None, :]).reshape(-1).astype(np.uint32)
+    rng = np.random.default_rng(77)
+    rand = rng.integers(0, 2 ** 32, 4_000_000, dtype=np.uint64).astype(np.uint32)
+    for bitsv in (near, rand):
+        x = bitsv.view(np.float32)
+        x = np.concatenate([x, -x])
+        assert np.array_equal(e4m3_encode(x), e4m3_encode_by_spacing(x))

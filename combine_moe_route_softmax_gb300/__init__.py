@@ -62,6 +62,7 @@ _SIGS = {
     "moe_quantize_weight_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_ex": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gemm_pairs": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_batched": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P],
                                  _I),
     "moe_grouped_gemm_combine": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I,
@@ -238,8 +239,9 @@ def moe_quantize_weight_fp8(w, stream=None):
 
 def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=None, w_extra=None,
                      w_extra_scales=None, epilogue=MOE_EPI_NONE, out=None, out_scales=None, dev_status=None,
-                     stream=None, row_scale=None):
-    """a [rows_cap, k] (bf16 or uint8 E4M3 codes); w [num_w, n, k]; returns (out, out_scales)."""
+                     stream=None, row_scale=None, pairs=False):
+    """a [rows_cap, k] (bf16 or uint8 E4M3 codes); w [num_w, n, k]; returns (out, out_scales).
+    pairs=True: the BF16 computation on pairs of SMs (moe_grouped_gemm_pairs)."""
     _dev(a)
     fp8 = a.dtype == torch.uint8
     rows_cap, k_dim = a.shape
@@ -252,7 +254,11 @@ def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=
         out = torch.empty(rows_cap, out_cols, dtype=odt, device=a.device)
     if fp8 and epilogue == MOE_EPI_SWIGLU and out_scales is None:
         out_scales = torch.empty(rows_cap, out_cols // 128, dtype=torch.float32, device=a.device)
-    if row_scale is None:
+    if pairs:
+        _check("moe_grouped_gemm_pairs", lib().moe_grouped_gemm_pairs(
+            _ptr(a), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), num_w, _ptr(w_extra), epilogue,
+            _ptr(out), _ptr(dev_status), _ptr(row_scale), _stream(stream)))
+    elif row_scale is None:
         _check("moe_grouped_gemm", lib().moe_grouped_gemm(
             _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
             num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),

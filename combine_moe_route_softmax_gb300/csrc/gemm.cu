@@ -886,7 +886,8 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
                               const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
                               moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
                               int32_t* dev_status, const float* row_scale, void* stream,
-                              const FuseIn* fuse = nullptr, unsigned long long timeout_ns = TIMEOUT_NS) {
+                              const FuseIn* fuse = nullptr, unsigned long long timeout_ns = TIMEOUT_NS,
+                              bool pairs = false) {
   const bool fp8 = dtype == MOE_E4M3;
   const bool swiglu = epilogue == MOE_EPI_SWIGLU;
   if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -939,8 +940,9 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   args.K = fuse ? fuse->K : 1;
   args.timeout_ns = timeout_ns;
   cudaStream_t s = as_stream(stream);
-  // BF16 without the fused combine: CTA pairs with the 2-SM MMA (gemm2sm.cu)
-  if (!fp8 && !fuse) {
+  // BF16 on CTA pairs with the 2-SM MMA (gemm2sm.cu), when asked for
+  if (pairs) {
+    if (fp8 || fuse) return MOE_ERR_UNSUPPORTED;
     args.stream = 1;
     args.common_off = 0;
     return launch_2sm(a, rows_cap, k_dim, n_dim, w, num_w, w_extra, swiglu, args, true, s);
@@ -994,18 +996,28 @@ extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales
                             w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream);
 }
 
-// Test hook, deliberately absent from the public header: moe_grouped_gemm_ex with the limit
-// of each pipeline wait given in nanoseconds instead of the built-in 2 s, so that a test can
-// make a wait run out and check the abort path (MOE_DEV_PIPELINE_TIMEOUT set, the call
-// returns, the next call is unaffected) without faulting or hanging anything.
+// Test hook, deliberately absent from the public header: moe_grouped_gemm_ex (pairs = 0) or
+// moe_grouped_gemm_pairs (pairs = 1) with the limit of each pipeline wait given in
+// nanoseconds instead of the built-in 2 s, so that a test can make a wait run out and check
+// the abort path (MOE_DEV_PIPELINE_TIMEOUT set, the call returns, the next call is
+// unaffected) without faulting or hanging anything.
 extern "C" moe_status_t moe_testing_grouped_gemm_wait_limit(
     const void* a, const float* a_scales, const int32_t* cu_seqlens, int num_segments, int rows_cap, int k_dim,
     int n_dim, const void* w, const float* w_scales, int num_w, const void* w_extra, const float* w_extra_scales,
     moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales, int32_t* dev_status,
-    const float* row_scale, unsigned long long wait_limit_ns, void* stream) {
+    const float* row_scale, unsigned long long wait_limit_ns, int pairs, void* stream) {
   return moe::gg::gemm_impl(a, a_scales, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, w_scales, num_w,
                             w_extra, w_extra_scales, dtype, epilogue, out, out_scales, dev_status, row_scale, stream,
-                            nullptr, wait_limit_ns);
+                            nullptr, wait_limit_ns, pairs != 0);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_pairs(const void* a, const int32_t* cu_seqlens, int num_segments,
+                                               int rows_cap, int k_dim, int n_dim, const void* w, int num_w,
+                                               const void* w_extra, moe_epilogue_t epilogue, void* out,
+                                               int32_t* dev_status, const float* row_scale, void* stream) {
+  return moe::gg::gemm_impl(a, nullptr, cu_seqlens, 0, num_segments, rows_cap, k_dim, n_dim, w, nullptr, num_w,
+                            w_extra, nullptr, MOE_BF16, epilogue, out, nullptr, dev_status, row_scale, stream, nullptr,
+                            moe::gg::TIMEOUT_NS, true);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_combine(

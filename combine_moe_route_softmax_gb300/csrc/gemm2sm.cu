@@ -1,4 +1,10 @@
-// BF16 grouped GEMM on CTA pairs with the 2-SM MMA (tcgen05.mma.cta_group::2).
+// BF16 grouped GEMM on CTA pairs with the 2-SM MMA (tcgen05.mma.cta_group::2), behind
+// moe_grouped_gemm_pairs.  It computes the same products in the same order as the
+// single-CTA kernel (gemm.cu), and its output is identical bit for bit.  Measured on GB300:
+// per SM its MMA pipeline runs a K step in 0.36 us against 0.40 us, but its streaming role
+// moves about half the bytes per SM, so on the prefill expert mix it is slower (gate/up 4.5
+// against 3.6 ms); on dense experts it ties or wins (down projection of 64 experts x 200
+// rows: 0.351 against 0.407 ms).  The layer uses the single-CTA kernel.
 //
 // MoonEP page: the experts run as grouped matmuls (gate, up, down) over the cu_seqlens
 // segments.  This kernel computes them for BF16 operands on pairs of CTAs (clusters of two
@@ -20,17 +26,22 @@
 //     SwiGLU rank r holds gate rows [128 nt + 64 r, +64) and the matching up rows, so its
 //     tensor memory lanes 0-63 hold g and lanes 64-127 u of the same 64 output columns.
 //
-// Hand-offs inside a pair.  Rank 0 (the leader) issues every MMA.  Each CTA's TMA copies
-// complete on its own full barrier; rank 1's copy completion is relayed to the leader by
-// one thread (a remote mbarrier arrive), so each CTA always knows when its own copies have
-// landed.  The leader's tcgen05.commit arrives on both CTAs' empty (stage free) and tfull
+// Hand-offs inside a pair.  Rank 0 (the leader) issues every MMA.  Both CTAs' TMA copies of
+// a stage complete on the leader's full barrier (the CTA-pair form of the copy may signal a
+// barrier of either CTA of the pair), which the leader's producer arms with the bytes of
+// both.  The leader's tcgen05.commit arrives on both CTAs' empty (stage free) and tfull
 // (accumulator ready) barriers; the epilogue warps of both CTAs arrive on the leader's
-// tempty barrier (accumulator drained).
+// tempty barrier (accumulator drained).  A stage thus costs one cross-CTA hop each way.
+// (A first version had rank 1's copies complete on its own barrier and one thread pass each
+// completion on with a remote arrive: that hop, paid once per stage, held both roles to
+// about 0.8-1.1 us per K step.)
 //
 // Every mbarrier wait is bounded (Args::timeout_ns of globaltimer); on expiry a CTA sets
-// MOE_DEV_PIPELINE_TIMEOUT, raises its own and its partner's abort flag, every role leaves
-// its loop, the producers wait (bounded) for their copies in flight, the leader waits
-// (bounded) for its MMAs, both CTAs meet at a cluster barrier and free the tensor memory.
+// MOE_DEV_PIPELINE_TIMEOUT, raises its own and its partner's abort flag and every role leaves
+// its loop.  The leader then waits (bounded) for the stages it armed, which covers both
+// CTAs' copies of those stages, and for its MMAs; rank 1, whose copies it cannot observe
+// itself, waits a grace period of 1 ms (copies of a few tens of KB land within microseconds)
+// before both CTAs meet at a cluster barrier and free the tensor memory.
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -45,6 +56,14 @@ constexpr int Q_STAGE_BYTES = B_HALF + QT_BYTES;     // 18 KB, a multiple of 102
 constexpr int Q_EPI_WARPS = 4;
 constexpr int Q_XPITCH = 17;                         // floats per lane row of the exchange (conflict-free)
 constexpr int NBAR_STAGES = Q_STAGES > P_STAGES ? Q_STAGES : P_STAGES;
+constexpr unsigned long long DRAIN_NS = 20000000ull;   // waits for work already in flight
+// Streaming pairs prefetch their weight boxes this many K blocks ahead of the loads into L2
+// (into the pair's next unit near the end of one): a stage waits for both CTAs' copies, so
+// the slower of two HBM trips sets its pace, and an L2 hit shortens it (gate/up on the
+// prefill mix 4.82 -> 4.49 ms of streaming; the single-CTA streaming role ran slower with the
+// same prefetch and does not use it).
+constexpr int STREAM_PREFETCH_KB = 16;
+constexpr unsigned long long GRACE_NS = 1000000ull;    // rank 1's wait for its own copies after an abort
 
 struct PairSmem {
   // MMA pipeline
@@ -57,10 +76,9 @@ struct PairSmem {
   static constexpr int q_xch = Q_STAGES * Q_STAGE_BYTES;
   static constexpr int y_end = q_xch + 2 * 2 * 32 * Q_XPITCH * 4;
   static constexpr int common_off = x_end > y_end ? x_end : y_end;
-  // common tail: barriers full[S], empty[S], pfull[S], tfull[2], tempty[2], drain; TMEM
-  // slot; abort flag; modelled role times; then int bnd[nseg + 1], prefix[nseg + 1],
-  // prefix_y[nseg + 1]
-  static constexpr int n_bars = 3 * NBAR_STAGES + 5;
+  // common tail: barriers full[S], empty[S], tfull[2], tempty[2], drain; TMEM slot; abort
+  // flag; modelled role times; then int bnd[nseg + 1], prefix[nseg + 1], prefix_y[nseg + 1]
+  static constexpr int n_bars = 2 * NBAR_STAGES + 5;
   static constexpr int tmem_slot = n_bars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int costs = abort_flag + 4;
@@ -75,8 +93,10 @@ static_assert(Q_STAGE_BYTES % 1024 == 0 && P_STAGE_TX % 1024 == 0, "swizzle atom
 // Modelled time of one pair-unit (relative; all units of a launch have the same K): two
 // M-tiles of a segment with more than one M-tile, the single M-tile of a short segment on
 // the MMA pipeline (its 256 weight rows stream from HBM behind a shallow ring), and a
-// streamed segment.  They set how many pairs stream.
-constexpr float COSTP_MMA = 38.0f, COSTP_SINGLE = 50.0f, COSTP_STREAM = 28.0f;
+// streamed segment.  They set how many pairs stream.  Measured per unit on the prefill
+// expert mix with both roles running (gate/up: about 40 us per pipeline unit, 47 us per
+// streamed unit).
+constexpr float COSTP_MMA = 40.0f, COSTP_SINGLE = 45.0f, COSTP_STREAM = 47.0f;
 
 // ------------------------------------------------------------------ cluster / pair PTX
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -105,6 +125,30 @@ __device__ __forceinline__ uint32_t map_to(uint32_t local, uint32_t rank) {
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA copy into this CTA's shared memory that completes on `bar`, a barrier of either CTA
+// of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                      uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+// Bounded wait for work already in flight (after an abort, or at the end).
+__device__ __forceinline__ void pdrain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > DRAIN_NS) return;
+  }
 }
 __device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
@@ -191,10 +235,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(cmn);
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return smem_u32(bars + NBAR_STAGES + s); };
-  auto bar_pfull = [&](int s) { return smem_u32(bars + 2 * NBAR_STAGES + s); };
-  auto bar_tfull = [&](int b) { return smem_u32(bars + 3 * NBAR_STAGES + b); };
-  auto bar_tempty = [&](int b) { return smem_u32(bars + 3 * NBAR_STAGES + 2 + b); };
-  const uint32_t bar_drain = smem_u32(bars + 3 * NBAR_STAGES + 4);
+  auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * NBAR_STAGES + b); };
+  auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * NBAR_STAGES + 2 + b); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * NBAR_STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cmn + PairSmem::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cmn + PairSmem::abort_flag);
   float* costs = reinterpret_cast<float*>(cmn + PairSmem::costs);
@@ -307,7 +350,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < NBAR_STAGES; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
-      mbar_init(bar_pfull(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -370,6 +412,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       uint64_t wpol;
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(wpol));
+      const uint32_t lead_full = map_to(bar_full(0), 0);
       for (int u = u_first; ok && u < u_end; u += u_step) {
         int seg, nt, row0;
         if (y_role) {
@@ -383,35 +426,65 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const bool extra = seg >= args.num_w;
         const int wbase = extra ? 0 : seg * args.n_dim;
+        // streaming: this CTA's weight boxes of this unit and of its next one, prefetched into
+        // L2 STREAM_PREFETCH_KB K blocks ahead of the loads
+        const CUtensorMap* pm = nullptr;
+        const CUtensorMap* npm = nullptr;
+        int p0 = 0, p1 = -1, n0 = -1, n1 = -1;
+        if (y_role) {
+          pm = SWIGLU ? (extra ? &tmBxh : &tmBh) : (extra ? &tmBx : &tmB);
+          p0 = SWIGLU ? wbase + nt * 128 + 64 * static_cast<int>(crank) : wbase + nt * BN + 128 * static_cast<int>(crank);
+          p1 = SWIGLU ? p0 + args.n_dim / 2 : -1;
+          if (u + u_step < u_end) {
+            int s2, nt2;
+            y_unit(u + u_step, s2, nt2);
+            const bool x2 = s2 >= args.num_w;
+            const int wb2 = x2 ? 0 : s2 * args.n_dim;
+            npm = SWIGLU ? (x2 ? &tmBxh : &tmBh) : (x2 ? &tmBx : &tmB);
+            n0 = SWIGLU ? wb2 + nt2 * 128 + 64 * static_cast<int>(crank) : wb2 + nt2 * BN + 128 * static_cast<int>(crank);
+            n1 = SWIGLU ? n0 + args.n_dim / 2 : -1;
+          }
+        }
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (y_role) {
+            const int pk = kb + STREAM_PREFETCH_KB;
+            if (pk < kblocks) {
+              tma_prefetch_2d(pm, pk * KE, p0);
+              if (p1 >= 0) tma_prefetch_2d(pm, pk * KE, p1);
+            } else if (n0 >= 0 && pk - kblocks < kblocks) {
+              tma_prefetch_2d(npm, (pk - kblocks) * KE, n0);
+              if (n1 >= 0) tma_prefetch_2d(npm, (pk - kblocks) * KE, n1);
+            }
+          }
           if (!pwait<false>(bar_empty(stage), phase ^ 1, ab)) {
             ok = false;
             break;
           }
           armed |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          // every copy of the stage completes on the leader's full barrier, armed there with
+          // the bytes of both CTAs
+          const uint32_t fb = lead_full + 8u * stage;
+          if (leader) mbar_expect_tx(bar_full(stage), 2 * (y_role ? Q_STAGE_BYTES : P_STAGE_TX));
           if (y_role) {
-            mbar_expect_tx(bar_full(stage), Q_STAGE_BYTES);
             const uint32_t sw = sbase + stage * Q_STAGE_BYTES;
             if (SWIGLU) {
               // 64 gate rows and the matching 64 up rows of this CTA's output columns
               const CUtensorMap* mh = extra ? &tmBxh : &tmBh;
               const int g0 = wbase + nt * 128 + 64 * static_cast<int>(crank);
-              tma_load_2d_hint(sw, mh, kb * KE, g0, bar_full(stage), wpol);
-              tma_load_2d_hint(sw + B_HALF / 2, mh, kb * KE, g0 + args.n_dim / 2, bar_full(stage), wpol);
+              tma_load_2d_pair_hint(sw, mh, kb * KE, g0, fb, wpol);
+              tma_load_2d_pair_hint(sw + B_HALF / 2, mh, kb * KE, g0 + args.n_dim / 2, fb, wpol);
             } else {
               const CUtensorMap* mb = extra ? &tmBx : &tmB;
-              tma_load_2d_hint(sw, mb, kb * KE, wbase + nt * BN + 128 * static_cast<int>(crank), bar_full(stage),
-                               wpol);
+              tma_load_2d_pair_hint(sw, mb, kb * KE, wbase + nt * BN + 128 * static_cast<int>(crank), fb, wpol);
             }
-            tma_load_2d(sw + B_HALF, &tmAq, kb * KE, row0, bar_full(stage));
+            tma_load_2d_pair(sw + B_HALF, &tmAq, kb * KE, row0, fb);
           } else {
-            mbar_expect_tx(bar_full(stage), P_STAGE_TX);
             const CUtensorMap* mb = extra ? &tmBx : &tmB;
             const int rb = SWIGLU ? wbase + (crank ? args.n_dim / 2 : 0) + nt * 128
                                   : wbase + nt * BN + 128 * static_cast<int>(crank);
-            tma_load_2d(sbase + PairSmem::a + stage * A_BYTES, &tmA, kb * KE, row0, bar_full(stage));
-            tma_load_2d(sbase + PairSmem::b + stage * B_HALF, mb, kb * KE, rb, bar_full(stage));
+            tma_load_2d_pair(sbase + PairSmem::a + stage * A_BYTES, &tmA, kb * KE, row0, fb);
+            tma_load_2d_pair(sbase + PairSmem::b + stage * B_HALF, mb, kb * KE, rb, fb);
           }
           if (++stage == nst) {
             stage = 0;
@@ -420,14 +493,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok) {
-        // wait for this CTA's copies still in flight before its shared memory goes away
-        for (int s = 0; s < nst; ++s)
-          if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
+        // copies still in flight land before this CTA's shared memory goes away: the leader
+        // sees both CTAs' copies of every stage it armed complete on its barriers; rank 1
+        // cannot observe its own, and gives them a grace period
+        if (leader) {
+          for (int s = 0; s < nst; ++s)
+            if (armed & (1u << s)) pdrain(bar_full(s), (last_parity >> s) & 1u);
+        } else {
+          const unsigned long long t0 = globaltimer();
+          while (globaltimer() - t0 < GRACE_NS) {
+          }
+        }
       } else {
         // every stage this CTA filled has been released by the leader's MMAs: no MMA reads
         // this CTA's shared memory any more and no commit is still on its way here
         for (int s = 0; s < nst; ++s)
-          if (armed & (1u << s)) mbar_drain(bar_empty(s), (last_parity >> s) & 1u);
+          if (armed & (1u << s)) pdrain(bar_empty(s), (last_parity >> s) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -447,7 +528,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
           }
-          if (!pwait<false>(bar_full(stage), phase, ab) || !pwait<true>(bar_pfull(stage), phase, ab)) {
+          if (!pwait<false>(bar_full(stage), phase, ab)) {
             ok = false;
             break;
           }
@@ -482,25 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) {
         tc2_commit(bar_drain);  // arrives once every MMA issued so far has completed
-        mbar_drain(bar_drain, 0);
-      }
-    } else if (lane == 0) {
-      // ------------------------------------------- relay (rank 1): own copies -> leader
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = u_first; ok && u < u_end; u += u_step) {
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!pwait<false>(bar_full(stage), phase, ab)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_remote(map_to(bar_pfull(stage), 0));
-          if (++stage == nst) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        pdrain(bar_drain, 0);
       }
     }
   } else if (!y_role) {

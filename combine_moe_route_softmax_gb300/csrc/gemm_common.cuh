@@ -1,6 +1,7 @@
-// Shared pieces of the tcgen05 grouped GEMM kernels (gemm.cu: one CTA per tile, used for
-// E4M3 and the fused combine; gemm2sm.cu: CTA pairs with the 2-SM MMA, used for BF16):
-// tile constants, launch arguments, PTX wrappers, the unit decoder.  Internal header.
+// Shared pieces of the tcgen05 grouped GEMM kernels (gemm.cu: one CTA per tile, behind
+// every grouped-GEMM call and the layer; gemm2sm.cu: BF16 on CTA pairs with the 2-SM MMA,
+// behind moe_grouped_gemm_pairs): tile constants, launch arguments, PTX wrappers, the unit
+// decoder.  Internal header.
 #pragma once
 
 #include <cuda.h>
@@ -29,6 +30,7 @@ constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
 
 constexpr int SMEM_MAX = 227 * 1024;
 constexpr int NS = 32;   // rows of a segment computed on the streaming CTAs (at most)
+
 
 struct Args {
   const int32_t* cu;        // cu_seqlens [nseg + 1], or masked_m [nseg] when max_tokens > 0
@@ -118,6 +120,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+// Prefetch of one box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 // With an L2 cache policy (createpolicy) attached to the copy.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,

@@ -59,7 +59,7 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 /* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
  * dispatch fake-quant options, 3 the batched expert layout, 4 the NVFP4 combine
  * and dispatch fake-quant (moe_combine_nvfp4, the dispatch_format arguments,
- * moe_layer_desc_t.combine_fq_format / dispatch_fq_format). */
+ * moe_layer_desc_t.combine_fq_format / dispatch_fq_format), 5 moe_grouped_gemm_pairs). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -222,6 +222,20 @@ moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int
                                  const void* w_extra, const float* w_extra_scales,
                                  moe_dtype_t dtype, moe_epilogue_t epilogue, void* out, float* out_scales,
                                  int32_t* dev_status, const float* row_scale, void* stream);
+
+/* moe_grouped_gemm_ex for BF16 computed on pairs of SMs (ABI 5): each 256-row M tile is
+ * split over the two CTAs of a 2-CTA cluster, which share one 256-wide weight tile through
+ * the 2-SM tensor-core MMA ([MoonEP] "Purpose": the gate, up and down grouped matmuls over
+ * the cu_seqlens segments).  Same arguments, layouts and results as moe_grouped_gemm_ex with
+ * dtype MOE_BF16 (the output is identical bit for bit); segments of at most 32 rows run on
+ * weight-streaming pairs when the launch has many units.  Which of the two is faster depends
+ * on the segment mix: on a mix of a few large and many tiny segments (the Zipf-routed prefill
+ * batch) this one is slower, on dense segments of a few hundred rows it is as fast or faster;
+ * moe_layer_forward uses moe_grouped_gemm_ex.  Errors as moe_grouped_gemm_ex. */
+moe_status_t moe_grouped_gemm_pairs(const void* a, const int32_t* cu_seqlens, int num_segments, int rows_cap,
+                                    int k_dim, int n_dim, const void* w, int num_w, const void* w_extra,
+                                    moe_epilogue_t epilogue, void* out, int32_t* dev_status,
+                                    const float* row_scale, void* stream);
 
 /* ------------------------------------------------------------ batched expert layout
  * The expert-batched activation format ([DeepEP]: the low-latency dispatch hands the

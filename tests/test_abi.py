@@ -39,7 +39,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_host_only_calls(lib):
-    assert lib.moe_abi_version() == 4
+    assert lib.moe_abi_version() == 5
     assert lib.moe_status_string(2) == b"workspace too small"
     # scratch sized from the inputs: grows with T, K and E
     a = lib.moe_permute_workspace_bytes(128, 8, 256, 1)

@@ -1,5 +1,6 @@
 """GPU parity of the tcgen05 grouped GEMM (BF16 and E4M3 with 128-block scales; plain and
-SwiGLU epilogues) against fp64 per-segment products computed by the oracle side, on
+SwiGLU epilogues; BF16 also on pairs of SMs) against fp64 per-segment products computed by
+the oracle side, on
 ragged segments: empty segments, tails shorter than a tile, a partial 128-column tile,
 the extra (shared-expert) segment, and more tiles than SMs so CTAs loop."""
 import numpy as np
@@ -53,9 +54,10 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("pairs", [False, True], ids=["cta", "pairs"])
 @pytest.mark.parametrize("swiglu", [False, True])
 @pytest.mark.parametrize("case", CASES, ids=range(len(CASES)))
-def test_bf16(case, swiglu):
+def test_bf16(case, swiglu, pairs):
     need_gpu()
     cu, rows_cap, k, n, num_w, extra = case
     if swiglu and n % 256:
@@ -66,7 +68,8 @@ def test_bf16(case, swiglu):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
     moe.moe_grouped_gemm(a.cuda(), cu_t, w.cuda(), w_extra=None if wx is None else wx.cuda(),
-                         epilogue=moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE, out=out, dev_status=st)
+                         epilogue=moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE, out=out, dev_status=st,
+                         pairs=pairs)
     torch.cuda.synchronize()
     assert st.item() == 0
     f = lambda t: bf16_bits_to_f32(bits(t)).astype(np.float64)
@@ -158,9 +161,10 @@ STREAM_CASES = [
 ]
 
 
+@pytest.mark.parametrize("pairs", [False, True], ids=["cta", "pairs"])
 @pytest.mark.parametrize("swiglu,layout,n,n_big,big_rows", STREAM_CASES,
                          ids=[f"{'swiglu' if c[0] else 'plain'}-{c[1]}-n{c[2]}" for c in STREAM_CASES])
-def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_rows):
+def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_rows, pairs):
     """Enough units per CTA that the launch splits its CTAs: segments of at most 32 rows go
     to streaming CTAs (weights as the MMA's M operand, the segment's rows as N = 32), the
     rest to the MMA pipeline.  Covers a short extra (shared-expert) segment, empty segments,
@@ -186,9 +190,11 @@ def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_row
         rs = None if swiglu else torch.rand(rows, generator=g) + 0.5
         out = torch.full((rows, cols), SENTINEL, dtype=torch.int16).view(torch.bfloat16).cuda()
         moe.moe_grouped_gemm(a.cuda(), torch.from_numpy(cu).cuda(), w.cuda(), w_extra=wx.cuda(), epilogue=epi,
-                             out=out, dev_status=st, row_scale=None if rs is None else rs.cuda())
+                             out=out, dev_status=st, row_scale=None if rs is None else rs.cuda(), pairs=pairs)
         spans = [(int(cu[s]), int(cu[s + 1]), int(cu[s + 1])) for s in range(S)]
     else:
+        if pairs:
+            pytest.skip("the pair computation takes contiguous segments")
         mt = 1024
         a = torch.randn(S, mt, k, generator=g).to(torch.bfloat16)
         rs = None if swiglu else torch.rand(S * mt, generator=g) + 0.5
@@ -216,3 +222,24 @@ def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_row
         scale = np.abs(acc).max()
         err = np.abs(f(ob[b:e]) - acc)
         assert np.all(err <= 2.0 ** -8 * np.abs(acc) + 2e-3 * scale), (s, e - b, err.max() / scale)
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_pairs_and_single_cta_agree_bit_for_bit(swiglu):
+    """The two BF16 computations accumulate the same products in the same order: identical
+    output on a mix of long, ragged and streamed segments."""
+    need_gpu()
+    k, n = 512, 1024
+    counts = streamed_counts(3, 12, 1500, 80)
+    cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    g = torch.Generator().manual_seed(21)
+    a = torch.randn(int(cu[-1]), k, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(len(counts), n, k, generator=g) / k ** 0.5).to(torch.bfloat16).cuda()
+    epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE
+    cu_t = torch.from_numpy(cu).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, _ = moe.moe_grouped_gemm(a, cu_t, w, epilogue=epi, dev_status=st)
+    o2, _ = moe.moe_grouped_gemm(a, cu_t, w, epilogue=epi, dev_status=st, pairs=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))

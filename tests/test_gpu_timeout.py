@@ -1,7 +1,7 @@
 """The grouped GEMM's failure detection, exercised without faulting or hanging anything:
-every pipeline wait of the kernel is bounded, and a wait that runs out sets
+every pipeline wait of the kernels is bounded, and a wait that runs out sets
 MOE_DEV_PIPELINE_TIMEOUT in the device status word, makes every role of the CTA (and of
-its partner CTA, for the BF16 CTA pairs) leave its loop, waits for the copies and MMAs
+its partner CTA, for the BF16 computation on SM pairs) leave its loop, waits for the copies and MMAs
 still in flight, frees the tensor memory and returns.  A test-only export of the library
 (absent from the public header) runs one grouped GEMM with a wait limit of a few
 nanoseconds, so that the first wait that is not satisfied at once runs out; the call must
@@ -27,7 +27,7 @@ I32 = ctypes.c_int
 def wait_limit_fn():
     f = moe.lib().moe_testing_grouped_gemm_wait_limit
     f.restype = I32
-    f.argtypes = [P, P, P, I32, I32, I32, I32, P, P, I32, P, P, I32, I32, P, P, P, P, ctypes.c_ulonglong, P]
+    f.argtypes = [P, P, P, I32, I32, I32, I32, P, P, I32, P, P, I32, I32, P, P, P, P, ctypes.c_ulonglong, I32, P]
     return f
 
 
@@ -35,17 +35,18 @@ def ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def run(f, a, a_s, cu, w, w_s, dtype, epi, out, out_s, st, limit_ns):
+def run(f, a, a_s, cu, w, w_s, dtype, epi, out, out_s, st, limit_ns, pairs):
     stream = torch.cuda.current_stream().cuda_stream
     rc = f(ptr(a), ptr(a_s), ptr(cu), cu.numel() - 1, a.shape[0], a.shape[1], w.shape[1], ptr(w), ptr(w_s),
-           w.shape[0], None, None, dtype, epi, ptr(out), ptr(out_s), ptr(st), None, limit_ns, stream)
+           w.shape[0], None, None, dtype, epi, ptr(out), ptr(out_s), ptr(st), None, limit_ns, int(pairs), stream)
     assert rc == 0, rc
 
 
-@pytest.mark.parametrize("fp8", [False, True], ids=["bf16-pairs", "e4m3"])
+@pytest.mark.parametrize("kind", ["bf16", "bf16-pairs", "e4m3"])
 @pytest.mark.parametrize("swiglu", [False, True], ids=["plain", "swiglu"])
-def test_wait_that_runs_out_aborts_cleanly(fp8, swiglu):
+def test_wait_that_runs_out_aborts_cleanly(kind, swiglu):
     need_gpu()
+    fp8, pairs = kind == "e4m3", kind == "bf16-pairs"
     f = wait_limit_fn()
     g = torch.Generator().manual_seed(5)
     cu = torch.tensor([0, 300, 300, 1000], dtype=torch.int32)
@@ -72,18 +73,18 @@ def test_wait_that_runs_out_aborts_cleanly(fp8, swiglu):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     # a fresh run with the built-in limit
     ref_out, ref_s = mk_out(), mk_s()
-    run(f, A, A_s, cu_d, W, W_s, dtype, epi, ref_out, ref_s, st, 2_000_000_000)
+    run(f, A, A_s, cu_d, W, W_s, dtype, epi, ref_out, ref_s, st, 2_000_000_000, pairs)
     torch.cuda.synchronize()
     assert st.item() == 0
     # a limit of a few nanoseconds: the first wait that is not satisfied at once runs out
     out, out_s = mk_out(), mk_s()
-    run(f, A, A_s, cu_d, W, W_s, dtype, epi, out, out_s, st, 4)
+    run(f, A, A_s, cu_d, W, W_s, dtype, epi, out, out_s, st, 4, pairs)
     torch.cuda.synchronize()       # the call returned: nothing waits forever
     assert st.item() & moe.MOE_DEV_PIPELINE_TIMEOUT
     # the next ordinary call on the same stream is unaffected
     st.zero_()
     out2, out2_s = mk_out(), mk_s()
-    run(f, A, A_s, cu_d, W, W_s, dtype, epi, out2, out2_s, st, 2_000_000_000)
+    run(f, A, A_s, cu_d, W, W_s, dtype, epi, out2, out2_s, st, 2_000_000_000, pairs)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert torch.equal(out2.view(torch.uint8), ref_out.view(torch.uint8))

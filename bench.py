@@ -172,7 +172,8 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- our arm
-def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=None, weight_in_down=False):
+def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=None, weight_in_down=False,
+                   gemm_pairs=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -191,7 +192,7 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         dtype = moe.MOE_E4M3
     layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine,
                          weight_in_down=weight_in_down, combine_fq=w.fq_format, dispatch_fq=dispatch_fq or "e4m3",
-                         **kw)
+                         gemm_pairs=gemm_pairs, **kw)
     fq = None
     if w.fake_quant:
         # combine fake-quant: the constant scale 448 / amax (E4M3) or the per-tensor scale
@@ -295,6 +296,9 @@ def staged_step(st, w, events):
         assert L.moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, nseg, mt, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
                                           d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                           p(st["status"]), None, s) == 0
+    elif d.gemm_pairs:
+        assert L.moe_grouped_gemm_pairs(v.xp, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), d.E, p(tw[2]),
+                                        moe.MOE_EPI_SWIGLU, v.hs, p(st["status"]), None, s) == 0
     else:
         assert L.moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
                                   d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
@@ -314,6 +318,9 @@ def staged_step(st, w, events):
         assert L.moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, nseg, mt, d.I, d.H, p(tw[1]), p(tw[5]),
                                           d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None,
                                           p(st["status"]), wd_rows, s) == 0
+    elif d.gemm_pairs:
+        assert L.moe_grouped_gemm_pairs(v.hs, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), d.E, p(tw[3]),
+                                        moe.MOE_EPI_NONE, v.y, p(st["status"]), wd_rows, s) == 0
     else:
         assert L.moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]),
                                      d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
@@ -366,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
     w = synth.WORKLOADS[args.workload]
     max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
     st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine, args.dispatch_fq,
-                        args.weight_in_down)
+                        args.weight_in_down, args.gemm_pairs)
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -555,6 +562,8 @@ def run_ours(args, rank, world, local_rank):
                    "combine": ("fused into the down projection" if args.fuse_combine else "separate kernel") +
                               (f", {'NVFP4' if w.fq_format == 'nvfp4' else 'E4M3'} fake-quant at the calibrated "
                                f"constant scale {float(st['fq'].item()):.5g}" if w.fake_quant else ""),
+                   "gemm": ("grouped GEMMs on SM pairs (2-SM MMA)" if args.gemm_pairs
+                            else "grouped GEMMs one CTA per tile"),
                    "router_weight": ("applied in the down projection's epilogue (weighted rows; the combine sums)"
                                      if args.weight_in_down else "applied in the combine"),
                    "dispatch": (f"{'NVFP4' if args.dispatch_fq == 'nvfp4' else 'E4M3'} fake-quant of the "
@@ -685,6 +694,8 @@ def main():
     ap.add_argument("--dispatch-fq", nargs="?", const="e4m3", default=None, choices=["e4m3", "nvfp4"],
                     help="BF16 workloads: fake-quant of the routed experts' input rows, E4M3 (default) or NVFP4, "
                          "at a per-tensor scale from the batch's amax")
+    ap.add_argument("--gemm-pairs", action="store_true",
+                    help="BF16: both grouped GEMMs on SM pairs with the 2-SM MMA (moe_grouped_gemm_pairs)")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="run the combine inside the down projection (moe_grouped_gemm_combine)")
     ap.add_argument("--max-tokens", type=int, default=0,

@@ -30,7 +30,7 @@ class MoeError(RuntimeError):
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
                 ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I), ("combine_fq_format", _I),
-                ("dispatch_fq_format", _I)]
+                ("dispatch_fq_format", _I), ("gemm_pairs", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -388,9 +388,11 @@ class MoeLayer:
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
-                 weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3", dispatch_fq="e4m3"):
+                 weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3", dispatch_fq="e4m3",
+                 gemm_pairs=False):
         self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
-                              int(max_tokens), int(fuse_combine), _fmt(combine_fq), _fmt(dispatch_fq))
+                              int(max_tokens), int(fuse_combine), _fmt(combine_fq), _fmt(dispatch_fq),
+                              int(gemm_pairs))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

@@ -32,6 +32,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
       (d->fuse_combine != 0 && d->fuse_combine != 1) ||
       (d->combine_fq_format != 0 && d->combine_fq_format != 1) ||
       (d->dispatch_fq_format != 0 && d->dispatch_fq_format != 1) ||
+      (d->gemm_pairs != 0 && d->gemm_pairs != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -109,6 +110,7 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   if (fp8 && dispatch_scale) return MOE_ERR_UNSUPPORTED;   // the FP8 path already quantises the dispatch
   const bool fq4 = fq_scale && d->combine_fq_format == 1;
   if (fq4 && d->fuse_combine) return MOE_ERR_UNSUPPORTED;
+  if (d->gemm_pairs && (fp8 || d->max_tokens > 0 || d->fuse_combine)) return MOE_ERR_UNSUPPORTED;
   if (d->has_shared && (!w->shared_w13 || !w->shared_w2 ||
                         (fp8 && (!w->shared_w13_scales || !w->shared_w2_scales))))
     return MOE_ERR_ARG;
@@ -158,6 +160,19 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                     dev_status, dispatch_scale, wd ? topk_w : nullptr, wd ? v.row_weights : nullptr, 0, nullptr,
                     stream, v.counters, d->H / 128, d->dispatch_fq_format);
   if (st != MOE_OK) return st;
+  if (d->gemm_pairs) {
+    st = moe_grouped_gemm_pairs(v.xp, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, d->E, sx13, MOE_EPI_SWIGLU,
+                                v.hs, dev_status, nullptr, stream);
+    if (st != MOE_OK) return st;
+    st = moe_grouped_gemm_pairs(v.hs, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, d->E, sx2, MOE_EPI_NONE, v.y,
+                                dev_status, wd ? v.row_weights : nullptr, stream);
+    if (st != MOE_OK) return st;
+    if (fq4)
+      return moe_combine_nvfp4(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H,
+                               d->has_shared ? v.y : nullptr, v.shared_map, fq_scale, out, stream);
+    return moe_combine(v.y, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, d->H, d->has_shared ? v.y : nullptr,
+                       v.shared_map, fq_scale, out, stream);
+  }
   st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
                         sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
                         v.hs_scales, dev_status, stream);

@@ -402,6 +402,9 @@ typedef struct {
   int combine_fq_format; /* with a combine fake-quant scale: 0 E4M3 (moe_combine), 1 NVFP4
                             (moe_combine_nvfp4; not with fuse_combine) (ABI 4) */
   int dispatch_fq_format; /* with a dispatch fake-quant scale: 0 E4M3, 1 NVFP4 (ABI 4) */
+  int gemm_pairs;     /* 1: both grouped GEMMs on SM pairs (moe_grouped_gemm_pairs; BF16,
+                         contiguous layout, not with fuse_combine, else MOE_ERR_UNSUPPORTED);
+                         same output bit for bit; 0: moe_grouped_gemm / _ex (ABI 5) */
 } moe_layer_desc_t;
 
 typedef struct {

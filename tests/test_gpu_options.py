@@ -170,3 +170,36 @@ def test_dispatch_fake_quant_rejected_for_e4m3_layers():
     with pytest.raises(moe.MoeError) as e:
         moe.moe_permute(idx, 4, x, out_dtype=moe.MOE_E4M3, dispatch_scale=torch.ones(1, device="cuda"))
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("weight_in_down", [False, True])
+def test_layer_gemm_pairs_bit_identical(weight_in_down):
+    """gemm_pairs runs both grouped GEMMs on SM pairs: the layer output equals the default
+    layer's bit for bit (prefill shapes, reduced, with the shared expert and the skewed
+    routing that gives long and short segments); E4M3, the batched layout and the fused
+    combine are refused."""
+    need_gpu()
+    w = scaled(WORKLOADS["prefill"], T=1024, T_valid=768, E=32)
+    logits = synth.router_logits(w, 0, device="cuda")
+    x = synth.hidden(w, 0, device="cuda")
+    w13, w2, s13, s2 = synth.expert_weights(w, 0, device="cuda")
+    outs = []
+    for pairs in (False, True):
+        layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_BF16, w13=w13, w2=w2, shared_w13=s13, shared_w2=s2,
+                             weight_in_down=weight_in_down, gemm_pairs=pairs)
+        idx = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
+        wt = torch.empty(w.T, w.K, dtype=torch.float32, device="cuda")
+        out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n = torch.tensor([w.T_valid], dtype=torch.int32, device="cuda")
+        layer.forward(x, out, idx, wt, logits=logits, num_tokens=n, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    for kw in (dict(max_tokens=w.T), dict(fuse_combine=True)):
+        bad = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_BF16, w13=w13, w2=w2, shared_w13=s13, shared_w2=s2,
+                           gemm_pairs=True, **kw)
+        with pytest.raises(moe.MoeError):
+            bad.forward(x, outs[0], torch.empty(w.T, w.K, dtype=torch.int32, device="cuda"),
+                        torch.empty(w.T, w.K, dtype=torch.float32, device="cuda"), logits=logits)

@@ -61,7 +61,7 @@ struct SmemLayout {
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_BYTES;
   static constexpr int xch = b + STAGES * B_BYTES;            // float [2][128]
-  static constexpr int stage_out = xch + 2 * 128 * 4;         // per epilogue warp: 32 x 80 B
+  static constexpr int stage_out = xch + 2 * 128 * 4;         // per epilogue warp: 32 x 64 B
   static constexpr int x_end = stage_out + EPI_WARPS * STAGE_OUT_BYTES;
   // streaming CTAs: YSTAGES x [256 weight rows | NS token rows]
   static constexpr int y_end = YSTAGES * YSTAGE_BYTES;
@@ -748,7 +748,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint4* my = reinterpret_cast<uint4*>(buf_w + lane * STAGE_OUT_PITCH);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t o[4];
@@ -756,14 +755,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 4; ++j)
               o[j] = (uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j]) |
                      ((uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j + 1]) << 16);
-            my[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(buf_w + stage_out_off(lane, v)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = (lane >> 2) + 8 * i;                 // row within the warp's 32
             const int ch = lane & 3;                           // 16-byte chunk of the row's 64 B
-            const uint4 val = *reinterpret_cast<const uint4*>(buf_w + r * STAGE_OUT_PITCH + 16 * ch);
+            const uint4 val = *reinterpret_cast<const uint4*>(buf_w + stage_out_off(r, ch));
             if (r < rows_here) {
               uint16_t* dst = static_cast<uint16_t*>(args.out) + (size_t)(w.row0 + 32 * q + r) * out_cols + col0 + 32 * c;
               reinterpret_cast<uint4*>(dst)[ch] = val;

@@ -25,8 +25,15 @@ constexpr int TMEM_COLS = 512;
 constexpr int MAX_SEG = kMaxExperts + 1;
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 
-constexpr int STAGE_OUT_PITCH = 80;                // 64 B of BF16 per row + 16 B pad (conflict-free)
+// Per-warp shared-memory transpose of the BF16 epilogue: 32 rows x 64 bytes (four 16-byte
+// chunks per row).  Chunk c of row r sits at chunk position c ^ ((r >> 1) & 3): a store of
+// chunk c by 8 consecutive rows, and a load of 2 consecutive rows' 4 chunks, each touch 32
+// distinct banks, so neither access conflicts.
+constexpr int STAGE_OUT_PITCH = 64;
 constexpr int STAGE_OUT_BYTES = 32 * STAGE_OUT_PITCH;
+__device__ __forceinline__ int stage_out_off(int row, int chunk) {
+  return row * STAGE_OUT_PITCH + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
 
 constexpr int SMEM_MAX = 227 * 1024;
 constexpr int NS = 32;   // rows of a segment computed on the streaming CTAs (at most)

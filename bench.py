@@ -538,7 +538,7 @@ def run_ours(args, rank, world, local_rank):
     cpu = (cpu_baseline(w, tokens=args.cpu_tokens, dispatch_fq=args.dispatch_fq)
            if world == 1 and not args.no_cpu_baseline else None)
     line = {
-        "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
+        "metric": "MoE layer tokens/s at 1 GB300; grouped-GEMM % TC peak; permute/combine % HBM BW",
         "value": round(whole_job_rate(w.T_valid, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -660,7 +660,7 @@ def run_reference(args, rank, world):
     v = round(args.ref_tokens / dt, 3)
     line = {
         "impl": "reference",
-        "metric": "MoE layer tokens/s at 1 GB300 (grouped-GEMM % TC peak, permute/combine % HBM BW in kernels)",
+        "metric": "MoE layer tokens/s at 1 GB300; grouped-GEMM % TC peak; permute/combine % HBM BW",
         "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)",

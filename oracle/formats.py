@@ -70,12 +70,18 @@ def _e4m3_value(c):
 
 # the value of every one of the 256 codes, from the definition above
 _E4M3_TABLE = _e4m3_value(np.arange(256, dtype=np.int64))
+_E4M3_TABLE64 = _E4M3_TABLE.astype(np.float64)
 
 
 def e4m3_decode(codes):
     """uint8 E4M3 codes -> float32 values (exact); codes 0x7F / 0xFF decode to NaN.
     A lookup in the table of all 256 code values."""
     return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_decode64(codes):
+    """e4m3_decode, as float64 (exact: every E4M3 value is a float32 and a float64)."""
+    return _E4M3_TABLE64[np.asarray(codes, dtype=np.uint8)]
 
 
 def e4m3_encode(x):
@@ -93,14 +99,25 @@ def e4m3_encode(x):
     x = np.ascontiguousarray(x, dtype=np.float32)
     u = x.view(np.uint32)
     mag = u & np.uint32(0x7FFFFFFF)
+    small = mag < np.uint32(0x3C800000)                          # below 2^-6
     nan = mag > np.uint32(0x7F800000)
-    kept = (mag + np.uint32(0x7FFFF) + ((mag >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)
-    norm = kept.view(np.int32) - np.int32((127 - 7) << 3)
-    sub = np.rint(np.abs(x) * np.float32(512.0)).astype(np.int32)
-    code = np.where(mag < np.uint32(0x3C800000), sub, norm)     # 0x3C800000 = 2^-6
-    code = np.minimum(code, np.int32(0x7E))
-    code = np.where(nan, np.int32(0x7F), code)
-    return (code | ((u >> np.uint32(24)) & np.uint32(0x80)).view(np.int32)).astype(np.uint8)
+    # normal range: round the dropped 20 bits to nearest even, then rebias the exponent
+    code = mag >> np.uint32(20)
+    code &= np.uint32(1)
+    code += mag
+    code += np.uint32(0x7FFFF)
+    code >>= np.uint32(20)
+    code = code.view(np.int32)
+    code -= np.int32((127 - 7) << 3)
+    # subnormal range: |x| * 2^9 rounded half to even
+    sub = np.abs(x)
+    sub *= np.float32(512.0)
+    np.rint(sub, out=sub)
+    np.copyto(code, sub.astype(np.int32), where=small)
+    np.minimum(code, np.int32(0x7E), out=code)
+    code[nan] = 0x7F
+    code |= ((u >> np.uint32(24)) & np.uint32(0x80)).view(np.int32)
+    return code.astype(np.uint8)
 
 
 def e4m3_round(x):

@@ -11,7 +11,8 @@ MoonEP page (after dispatch the rows arrive grouped by expert).
 """
 import numpy as np
 
-from .formats import (bf16_bits_to_f32, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode, f32_to_bf16_bits)
+from .formats import (bf16_bits_to_f32, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_decode64, e4m3_encode,
+                      f32_to_bf16_bits)
 
 F32 = np.float32
 STATUS_BAD_EXPERT = 1
@@ -212,8 +213,9 @@ def weight_quant_128x128(w):
 def dequant(codes, scales, block_rows):
     """codes * scale in float64, the scale block being block_rows x 128."""
     R, C = codes.shape
-    v = e4m3_decode(codes).astype(np.float64).reshape(R // block_rows, block_rows, C // 128, 128)
-    return (v * scales.astype(np.float64)[:, None, :, None]).reshape(R, C)
+    v = e4m3_decode64(codes).reshape(R // block_rows, block_rows, C // 128, 128)
+    v *= scales.astype(np.float64)[:, None, :, None]
+    return v.reshape(R, C)
 
 
 # --------------------------------------------------------------------------- experts
@@ -372,7 +374,8 @@ def _f64_weights(w_bits_or_f):
 
 
 def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
-                    fq_scale=None, fp8=False, dispatch_scale=None, fq_format="e4m3", dispatch_format="e4m3"):
+                    fq_scale=None, fp8=False, dispatch_scale=None, fq_format="e4m3", dispatch_format="e4m3",
+                    workers=None):
     """Dense per-token reference MoE in fp64 (the MoonEP page validates its path by
     comparing with a straightforward per-token MoE): for each token, for the valid slots in ascending
     order, r = w_k * expert_{idx_k}(x_t) (optionally fake-quantised as in the combine);
@@ -389,6 +392,8 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     unfused when the dispatch is quantised, since a fused one would read the same tokens).
     fq_format: the combine fake-quant's format when fq_scale is given, "e4m3" or "nvfp4";
     dispatch_format: the dispatch fake-quant's, likewise.
+    workers: how many experts to compute at once in threads (default 1); the result does
+    not depend on it.
     Returns float64 [len(tokens), H].
     """
     x = bf16_bits_to_f32(np.asarray(x_bits)).astype(np.float64)
@@ -404,10 +409,10 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
         return dequant(q, s, 1)
 
     def prep_w(wm):
-        wm = _f64_weights(wm)
         if not fp8:
-            return wm
-        q, s = weight_quant_128x128(wm.astype(F32))
+            return _f64_weights(wm)
+        wm = np.asarray(wm)
+        q, s = weight_quant_128x128(bf16_bits_to_f32(wm) if wm.dtype == np.uint16 else wm.astype(F32))
         return dequant(q, s, 128)
 
     def run_expert(xr, w13e, w2e):
@@ -426,12 +431,25 @@ def layer_reference(x_bits, topk_idx, topk_w, w13, w2, shared=None, tokens=None,
     if dispatch_scale is not None:
         xq = dispatch_qdq_bits(np.asarray(x_bits)[toks], dispatch_scale, dispatch_format)
         xs = prep_x(bf16_bits_to_f32(xq).astype(np.float64))
-    # expert outputs for every (token, slot) pair of the subset, one expert at a time
+    # expert outputs for every (token, slot) pair of the subset, expert by expert; the experts
+    # are independent, so up to `workers` of them run at once in threads (numpy's array
+    # operations release the interpreter lock), each computed exactly as when run alone
     contrib = np.zeros((len(toks), K, H), dtype=np.float64)
     sub_idx = topk_idx[toks]
-    for e in np.unique(sub_idx[sub_idx >= 0]):
+
+    def expert_rows(e):
         where = np.nonzero(sub_idx == e)
-        ye = run_expert(xs[where[0]], prep_w(w13[e]), prep_w(w2[e]))
+        return where, run_expert(xs[where[0]], prep_w(w13[e]), prep_w(w2[e]))
+
+    experts = np.unique(sub_idx[sub_idx >= 0])
+    n_workers = min(len(experts), workers if workers else 1)
+    if n_workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(n_workers) as pool:
+            results = list(pool.map(expert_rows, experts))
+    else:
+        results = [expert_rows(e) for e in experts]
+    for where, ye in results:
         contrib[where[0], where[1]] = ye
     out = np.zeros((len(toks), H), dtype=np.float64)
     wsub = np.asarray(topk_w, dtype=F32)[toks]

@@ -1,10 +1,12 @@
 """End-to-end GPU parity of moe_layer_forward against the oracle's dense per-token fp64
 reference, on every workload at its full size (a seeded 1024-token subset of the 8192
-prefill tokens, every decode token) and on reduced sizes checked token by token; the FP8
+prefill tokens, every decode token against both FP8 references) and on reduced sizes checked token by token; the FP8
 workload against both the unquantised BF16 masters and the FP8-quantised operands; the
 fake-quant workload with its calibration, captured and replayed in a CUDA graph after a
 padding-only warm-up, with the on-device combine check.  Each comparison prints its max
 relative error and its elementwise allclose fraction at atol = rtol = tolerance."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -19,6 +21,7 @@ from oracle.formats import bf16_bits_to_f32
 pytestmark = pytest.mark.gpu
 
 TOL = {"bf16": 2e-2, "e4m3": 6e-2}
+WORKERS = min(16, os.cpu_count() or 1)   # experts the oracle computes at once (threads)
 
 
 class Setup:
@@ -66,7 +69,7 @@ class Setup:
         shared = (bits(self.s13), bits(self.s2)) if self.w.shared else None
         return ref.layer_reference(bits(self.x), self.o_idx, self.o_w, ExpertBits(self.w13), ExpertBits(self.w2),
                                    shared=shared, tokens=tokens, fq_scale=fq_scale,
-                                   fp8=(self.w.dtype == "e4m3") if fp8 is None else fp8)
+                                   fp8=(self.w.dtype == "e4m3") if fp8 is None else fp8, workers=WORKERS)
 
 
 def allclose_fraction(got, want, tol):
@@ -159,14 +162,13 @@ def test_layer_prefill_full_size_sampled():
 
 
 def test_layer_decode_full_size_every_token():
-    """Full decode size, compared twice: a seeded subset against the fp64 layer on the
-    FP8-quantised operands at the FP8 tolerance 6e-2 (the oracle's FP8 quantisation of
-    every touched expert's weights is the slow part, so it runs on the experts of a few
-    tokens), and all 128 tokens against the fp64 layer on the unquantised BF16 masters at
+    """Full decode size, every one of the 128 tokens compared twice: against the fp64 layer
+    on the FP8-quantised operands at the FP8 tolerance 6e-2 (every touched expert's weights
+    quantised by the oracle), and against the fp64 layer on the unquantised BF16 masters at
     the bound E4M3's rounding allows (below)."""
     need_gpu()
     s = Setup(WORKLOADS["decode"])
-    check_layer(s, sample_tokens(128, 4, seed=2), TOL["e4m3"], label="decode vs the FP8-operand reference")
+    check_layer(s, np.arange(128), TOL["e4m3"], label="decode vs the FP8-operand reference")
     # Against the BF16 masters the difference is E4M3's own rounding: x, W13, h and W2 are
     # each rounded with a relative error of rms 2^-4 / sqrt(3) = 3.6 % (three mantissa
     # bits), which compounds to sqrt(4) * 3.6 % = 7.2 % rms on the output.  The oracle's FP8

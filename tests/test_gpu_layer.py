@@ -1,6 +1,6 @@
 """End-to-end GPU parity of moe_layer_forward against the oracle's dense per-token fp64
-reference, on every workload at its full size (a seeded 1024-token subset of the 8192
-prefill tokens, every decode token against both FP8 references) and on reduced sizes checked token by token; the FP8
+reference, on every workload at its full size (every one of the 8192 prefill tokens, every
+decode token against both FP8 references) and on reduced sizes checked token by token; the FP8
 workload against both the unquantised BF16 masters and the FP8-quantised operands; the
 fake-quant workload with its calibration, captured and replayed in a CUDA graph after a
 padding-only warm-up, with the on-device combine check.  Each comparison prints its max
@@ -119,12 +119,12 @@ def test_layer_every_token(name, T, H, I, E, K):
     check_layer(s, tokens, TOL[w.dtype])
 
 
-def test_layer_prefill_full_size_sampled():
-    """Full prefill size: a seeded subset of 1024 tokens against the fp64 reference (the
-    whole layer output is also checked as the re-sum of the layer's own expert rows)."""
+def test_layer_prefill_full_size_every_token():
+    """Full prefill size: all 8192 tokens against the fp64 reference (the whole layer
+    output is also checked as the re-sum of the layer's own expert rows)."""
     need_gpu()
     s = Setup(WORKLOADS["prefill"])
-    check_layer(s, sample_tokens(8192, 1024, seed=1), TOL["bf16"], label="prefill (1024 sampled tokens)")
+    check_layer(s, np.arange(8192), TOL["bf16"], label="prefill (every token)")
     # the expert-major layout the layer built is the oracle's, bit for bit
     v = s.layer.views
     cap = 16384 * 8 + 16384
@@ -251,14 +251,14 @@ def test_fake_quant_layer_in_cuda_graph():
     torch.cuda.synchronize()
     assert np.array_equal(bits(s.out), graph_out)
     assert np.array_equal(host(s.topk_idx), s.o_idx)
-    tokens = sample_tokens(8192, 1024, seed=3)
+    tokens = np.arange(8192)
     got = bf16_bits_to_f32(graph_out).astype(np.float64)[tokens]
     want = s.reference(tokens, fq_scale=np.float32(s_o))
-    err, _ = report("prefill_fq graph replay (1024 sampled tokens)", got, want, TOL["e4m3"])
+    err, _ = report("prefill_fq graph replay (every token)", got, want, TOL["e4m3"])
     assert err <= TOL["e4m3"], err
-    # fake-quant changed the output
-    plain = s.reference(tokens)
-    assert ref.max_rel_err(want, plain) > 1e-3
+    # fake-quant changed the output (on a sample of tokens)
+    few = sample_tokens(8192, 64, seed=3)
+    assert ref.max_rel_err(want[few], s.reference(few)) > 1e-3
     # a graph holding only the on-device check: rows that no longer reproduce the output
     # (a changed layout) set the mismatch bit on replay instead of asserting
     g2 = torch.cuda.CUDAGraph()

@@ -180,6 +180,8 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
     w13, w2, s13, s2 = synth.expert_weights(w, 0, device=device)   # weights shared by all ranks
     kw = dict(w13=w13, w2=w2, shared_w13=s13, shared_w2=s2)
     dtype = moe.MOE_BF16
+    if gemm_pairs and (w.dtype != "bf16" or max_tokens or fuse_combine):
+        raise SystemExit("--gemm-pairs applies to BF16 workloads in the contiguous layout without --fuse-combine")
     if w.dtype == "e4m3":
         q13, c13 = moe.moe_quantize_weight_fp8(w13)
         q2, c2 = moe.moe_quantize_weight_fp8(w2)

@@ -610,56 +610,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (SWIGLU) {
         if (row_ok && cols_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+          float h[64];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float h0 = silu(acc[8 * v + 2 * j]) * acc[64 + 8 * v + 2 * j];
-              const float h1 = silu(acc[8 * v + 2 * j + 1]) * acc[64 + 8 * v + 2 * j + 1];
-              o[j] = (uint32_t)f32_to_bf16(h0) | ((uint32_t)f32_to_bf16(h1) << 16);
-            }
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
+          for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
+          store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
         }
       } else if (cols_ok) {
-        // BF16 rows through a per-warp shared-memory transpose: each lane holds one row, but
-        // a store instruction should cover whole sectors, so each 32-column chunk is written
-        // to shared memory row by row and read back as 8 rows x 64 contiguous bytes
         if (args.row_scale) {
           // router weight of each permuted row, applied to the float32 accumulator
           const float rs = row_ok ? args.row_scale[row] : 0.0f;
 #pragma unroll
           for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
         }
-        uint8_t* buf_w = stage_out + (warp - 2) * STAGE_OUT_BYTES;
         const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              o[j] = (uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j]) |
-                     ((uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j + 1]) << 16);
-            *reinterpret_cast<uint4*>(buf_w + stage_out_off(lane, v)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = (lane >> 2) + 8 * i;                 // row within the warp's 32
-            const int ch = lane & 3;                           // 16-byte chunk of the row's 64 B
-            const uint4 val = *reinterpret_cast<const uint4*>(buf_w + stage_out_off(r, ch));
-            if (r < rows_here) {
-              uint16_t* dst =
-                  static_cast<uint16_t*>(args.out) + (size_t)(w.row0 + 32 * q + r) * out_cols + col0 + 32 * c;
-              reinterpret_cast<uint4*>(dst)[ch] = val;
-            }
-          }
-          __syncwarp();
-        }
+        store_rows_bf16(acc, stage_out + (warp - 2) * STAGE_OUT_BYTES, lane, rows_here,
+                        static_cast<uint16_t*>(args.out), w.row0 + 32 * q, out_cols, col0);
       }
     }
   } else if (warp < 2 + Q_EPI_WARPS) {

@@ -225,6 +225,53 @@ __host__ __device__ constexpr uint32_t instr_desc_stream() {
 // 2^126 and the quotient flushes to 0, the limit of g * sigmoid(g).
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// ------------------------------------------------------------- BF16 epilogue stores
+// SwiGLU: this thread's 64 values of h (one row, 64 consecutive output columns) as BF16,
+// 128 contiguous bytes at dst.
+__device__ __forceinline__ void store_h_bf16(const float (&h)[64], uint16_t* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = (uint32_t)f32_to_bf16(h[8 * v + 2 * j]) | ((uint32_t)f32_to_bf16(h[8 * v + 2 * j + 1]) << 16);
+    d[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+// Plain epilogue: the warp's 32 rows (lane = row) x 128 columns of acc as BF16 rows through
+// the per-warp shared-memory transpose (buf_w, STAGE_OUT_BYTES): each lane holds one row,
+// but a store instruction should cover whole sectors, so each 32-column chunk is written to
+// shared memory row by row and read back as 8 rows x 64 contiguous bytes.  Rows
+// [0, rows_here) of the warp are stored, row r at out + (row0 + r) * out_cols + col0.
+__device__ __forceinline__ void store_rows_bf16(const float (&acc)[128], uint8_t* buf_w, int lane, int rows_here,
+                                                uint16_t* out, int row0, int out_cols, int col0) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = (uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j]) |
+               ((uint32_t)f32_to_bf16(acc[32 * c + 8 * v + 2 * j + 1]) << 16);
+      *reinterpret_cast<uint4*>(buf_w + stage_out_off(lane, v)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (lane >> 2) + 8 * i;                 // row within the warp's 32
+      const int ch = lane & 3;                           // 16-byte chunk of the row's 64 B
+      const uint4 val = *reinterpret_cast<const uint4*>(buf_w + stage_out_off(r, ch));
+      if (r < rows_here) {
+        uint16_t* dst = out + (size_t)(row0 + r) * out_cols + col0 + 32 * c;
+        reinterpret_cast<uint4*>(dst)[ch] = val;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 struct Unit {
   int seg, row0, row_end, nt;
 };

@@ -109,11 +109,13 @@ def e4m3_encode(x):
     code >>= np.uint32(20)
     code = code.view(np.int32)
     code -= np.int32((127 - 7) << 3)
-    # subnormal range: |x| * 2^9 rounded half to even
-    sub = np.abs(x)
-    sub *= np.float32(512.0)
-    np.rint(sub, out=sub)
-    np.copyto(code, sub.astype(np.int32), where=small)
+    # subnormal range: |x| * 2^9 rounded half to even (computed for every element, used only
+    # where |x| < 2^-6; the others may overflow or be NaN, harmlessly)
+    with np.errstate(over="ignore", invalid="ignore"):
+        sub = np.abs(x)
+        sub *= np.float32(512.0)
+        np.rint(sub, out=sub)
+        np.copyto(code, sub.astype(np.int32), where=small)
     np.minimum(code, np.int32(0x7E), out=code)
     code[nan] = 0x7F
     code |= ((u >> np.uint32(24)) & np.uint32(0x80)).view(np.int32)

@@ -88,7 +88,8 @@ def e4m3_encode_by_spacing(x):
     float64 the spacing of E4M3 values around |x| is 2^-9 below 2^-6, else 2^(e-3) for
     2^e <= |x| < 2^(e+1); |x| / spacing is rounded half to even and scaled back, clamped
     to 448, and the code read off the rounded value."""
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):         # signalling NaN patterns among the inputs
+        x = np.asarray(x, dtype=np.float32).astype(np.float64)
     neg = np.signbit(x)
     a = np.abs(x)
     nan = np.isnan(a)
@@ -96,7 +97,8 @@ def e4m3_encode_by_spacing(x):
     _, ex = np.frexp(a)
     e = ex.astype(np.int64) - 1
     step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.exp2(np.maximum(e, -6) - 3.0))
-    v = np.minimum(np.rint(a / step) * step, 448.0)
+    with np.errstate(invalid="ignore"):         # infinities: inf / step, clamped to 448 below
+        v = np.minimum(np.rint(a / step) * step, 448.0)
     _, vex = np.frexp(v)
     ve = vex.astype(np.int64) - 1
     is_sub = v < 2.0 ** -6

@@ -165,7 +165,9 @@ def test_layer_decode_full_size_every_token():
     """Full decode size, every one of the 128 tokens compared twice: against the fp64 layer
     on the FP8-quantised operands at the FP8 tolerance 6e-2 (every touched expert's weights
     quantised by the oracle), and against the fp64 layer on the unquantised BF16 masters at
-    the bound E4M3's rounding allows (below)."""
+    the bound E4M3's rounding allows (below).  The 6e-2 figure is the MoonEP page's test
+    tolerance ("BF16 integration of MoonEP balanced EP backend", Test Result: atol = rtol =
+    6e-2 against a per-token reference MoE), set there for BF16 operands."""
     need_gpu()
     s = Setup(WORKLOADS["decode"])
     check_layer(s, np.arange(128), TOL["e4m3"], label="decode vs the FP8-operand reference")

@@ -18,8 +18,9 @@
 // the grid, BF16 and not fused, when the launch has at least 16 units per CTA) take the
 // segments of at most NS rows: such a segment is a weight stream, so its CTAs keep six
 // 32 KB weight tiles in flight behind 4 KB token tiles and issue MMAs with the weights as
-// the M = 128 operand and the segment's rows as N = NS.  Every CTA derives the same ny from
-// the segment lengths and a per-unit cost model, so no host sync is needed.
+// the M = 128 operand and the segment's rows as N = NS, on two pipeline lanes (two TMA
+// threads, two MMA threads, alternate K blocks).  Every CTA derives the same ny from the
+// segment lengths and a per-unit cost model, so no host sync is needed.
 //
 // Warp roles of the MMA pipeline (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane)
@@ -34,9 +35,12 @@
 //         float32 registers by the epilogue warps ("promotion"), since the scales are
 //         float32 per 128 elements rather than a format the MMA applies itself.
 //
+// Warp roles of a streaming CTA: warps 0 and 6 TMA producers of pipeline lanes 0 and 1,
+// warps 1 and 7 their MMA issuers (warp 1 also allocates TMEM), warps 2..5 epilogue.
+//
 // Every mbarrier wait is bounded (about 2 s of globaltimer); on expiry the CTA sets
-// MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producer
-// waits (bounded) for its copies in flight, the MMA lane waits (bounded) for its MMAs,
+// MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producers
+// wait (bounded) for their copies in flight, the MMA lanes wait (bounded) for their MMAs,
 // and the TMEM is freed before the CTA exits.
 #include "gemm_common.cuh"
 
@@ -66,9 +70,9 @@ struct SmemLayout {
   // streaming CTAs: YSTAGES x [256 weight rows | NS token rows]
   static constexpr int y_end = YSTAGES * YSTAGE_BYTES;
   // common tail at Args::common_off (after x_end, or after y_end when streaming is on):
-  // barriers full[6], empty[6], tfull[2], tempty[2], drain; TMEM slot; abort flag; role
+  // barriers full[6], empty[6], tfull[2], tempty[2], drain[2]; TMEM slot; abort flag; role
   // split; then int cu[nseg + 1], prefix[nseg + 1], prefix_y[nseg + 1]
-  static constexpr int n_bars = 2 * YSTAGES + 5;
+  static constexpr int n_bars = 2 * YSTAGES + 6;
   static constexpr int tmem_slot = n_bars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int costs = abort_flag + 4;                // float [2]
@@ -84,10 +88,12 @@ static_assert(STAGES <= YSTAGES, "barrier slots");
 // CTAs stream; measured per unit on the prefill expert mix with both roles running (gate/up:
 // 45.4 and 50.7 us; down: 12.9 and 14.8 us), the streamed cost rounded up so that the
 // streaming CTAs, which cannot hand work back, are not the last to finish.
-constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 53.5f;
+constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 42.0f;
 // Streaming CTAs: warp 0 loads the ring, warp 1 issues the MMAs, warps 2..5 are the
 // epilogue (one unit streams for tens of microseconds; its epilogue is short).
 constexpr int Y_EPI_WARPS = 4;
+constexpr int Y_PRODUCER1 = 2 + Y_EPI_WARPS, Y_ISSUER1 = Y_PRODUCER1 + 1;  // lane 1 of the streaming pipeline
+static_assert(Y_ISSUER1 < THREADS / 32, "streaming warps");
 // A streamed weight tile is read once: its copies carry an L2 evict-first policy, so the
 // streaming CTAs' gigabytes do not push out the weight tiles that the MMA pipeline's
 // M-tiles of one segment share through L2.
@@ -182,6 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * YSTAGES + b); };
   auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * YSTAGES + 2 + b); };
   const uint32_t bar_drain = smem_u32(bars + 2 * YSTAGES + 4);
+  const uint32_t bar_drain1 = smem_u32(bars + 2 * YSTAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cmn + SmemLayout::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cmn + SmemLayout::abort_flag);
   float* costs = reinterpret_cast<float*>(cmn + SmemLayout::costs);
@@ -297,10 +304,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tfull(b), y_role ? 2 : 1);   // streaming: one arrival per pipeline lane
       mbar_init(bar_tempty(b), y_role ? Y_EPI_WARPS : EPI_WARPS);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain1, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -334,8 +342,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ================================================ streaming CTA: segments of <= NS rows
       // Unit v: the t-th streamed segment (t = v / n_tiles) and N-tile nt = v % n_tiles.  The
       // two 128-row halves of the weight tile are the A operands of two MMAs (M = 128) that
-      // share the segment's NS token rows as B (N = NS); TMEM buffer b holds half 0's
-      // products in columns [2 NS b, +NS) and half 1's in the next NS columns.
+      // share the segment's NS token rows as B (N = NS).
+      // The K blocks of this CTA's units, numbered g = 0, 1, ... in order, run on two lanes
+      // of the pipeline: lane p (producer thread p, MMA thread p) takes the K blocks with
+      // g % 2 == p, which live in the stages of parity p (stage g % YSTAGES, YSTAGES even),
+      // and accumulates into its own TMEM columns; the epilogue adds lane 0's sum (even K
+      // blocks) and lane 1's (odd K blocks), in that order.  k_dim is a multiple of 128, so
+      // a unit has an even number of 64-wide K blocks and g % 2 == kb % 2.  A single MMA
+      // thread waits on a barrier between every two groups of eight short MMAs and the
+      // tensor pipe idles in those waits; two keep it busy.  TMEM buffer b, lane p: half 0's
+      // products in columns [4 NS b + 2 NS p, +NS), half 1's in the next NS columns.
       const int yi = static_cast<int>(blockIdx.x) - gx;
       auto y_unit = [&](int v, int& seg, int& nt) {
         const int t = v / n_tiles;
@@ -350,12 +366,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         seg = lo;
       };
-      if (warp == 0) {
+      if (warp == 0 || warp == Y_PRODUCER1) {
+        const uint32_t p = warp == 0 ? 0u : 1u;
         if (lane == 0) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmAt)) : "memory");
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
           int stage = 0;
-          uint32_t phase = 0, armed = 0, last_parity = 0;
+          uint32_t phase = 0, armed = 0, last_parity = 0, g = 0;
           bool ok = true;
           uint64_t wpol;
           asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(wpol));
@@ -368,23 +385,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int wbase = extra ? 0 : seg * args.n_dim;
             const int rA = SWIGLU ? wbase + nt * 128 : wbase + nt * BN;
             const int rB = SWIGLU ? wbase + args.n_dim / 2 + nt * 128 : rA + 128;
-            for (int kb = 0; kb < kblocks; ++kb) {
-              if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
-                ok = false;
-                break;
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+              if ((g & 1u) == p) {
+                if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+                  ok = false;
+                  break;
+                }
+                mbar_expect_tx(bar_full(stage), YSTAGE_BYTES);
+                armed |= 1u << stage;
+                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                const uint32_t sw = sbase + stage * YSTAGE_BYTES;
+                if (STREAM_EVICT_FIRST) {
+                  tma_load_2d_hint(sw, mb, kb * KE, rA, bar_full(stage), wpol);
+                  tma_load_2d_hint(sw + B_HALF, mb, kb * KE, rB, bar_full(stage), wpol);
+                } else {
+                  tma_load_2d(sw, mb, kb * KE, rA, bar_full(stage));
+                  tma_load_2d(sw + B_HALF, mb, kb * KE, rB, bar_full(stage));
+                }
+                tma_load_2d(sw + B_BYTES, &tmAt, kb * KE, row0, bar_full(stage));
               }
-              mbar_expect_tx(bar_full(stage), YSTAGE_BYTES);
-              armed |= 1u << stage;
-              last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-              const uint32_t sw = sbase + stage * YSTAGE_BYTES;
-              if (STREAM_EVICT_FIRST) {
-                tma_load_2d_hint(sw, mb, kb * KE, rA, bar_full(stage), wpol);
-                tma_load_2d_hint(sw + B_HALF, mb, kb * KE, rB, bar_full(stage), wpol);
-              } else {
-                tma_load_2d(sw, mb, kb * KE, rA, bar_full(stage));
-                tma_load_2d(sw + B_HALF, mb, kb * KE, rB, bar_full(stage));
-              }
-              tma_load_2d(sw + B_BYTES, &tmAt, kb * KE, row0, bar_full(stage));
               if (++stage == YSTAGES) {
                 stage = 0;
                 phase ^= 1;
@@ -396,52 +415,55 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
           }
         }
-      } else if (warp == 1) {
+      } else if (warp == 1 || warp == Y_ISSUER1) {
+        const uint32_t p = warp == 1 ? 0u : 1u;
         if (lane == 0) {
           constexpr uint32_t idesc = instr_desc_stream();
+          const uint32_t drain = p == 0 ? bar_drain : bar_drain1;
           int stage = 0, buf = 0;
-          uint32_t phase = 0, tphase = 0;
+          uint32_t phase = 0, tphase = 0, g = 0;
           bool ok = true;
           for (int v = yi; ok && v < total_y; v += ny) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-              if (kb == 0) {
-                if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+            if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dt = tmem_base + buf * (4 * NS) + p * (2 * NS);
+            bool first = true;
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+              if ((g & 1u) == p) {
+                if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-              }
-              if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t sw = sbase + stage * YSTAGE_BYTES;
-              const uint32_t st = sw + B_BYTES;
-              const uint32_t dt = tmem_base + buf * (2 * NS);
+                const uint32_t sw = sbase + stage * YSTAGE_BYTES;
+                const uint32_t st = sw + B_BYTES;
 #pragma unroll
-              for (int k = 0; k < KB_BYTES / 32; ++k) {
-                const uint32_t acc = (kb | k) != 0;
-                tc_mma<false>(dt, smem_desc(sw + 32 * k), smem_desc(st + 32 * k), idesc, acc);
-                tc_mma<false>(dt + NS, smem_desc(sw + B_HALF + 32 * k), smem_desc(st + 32 * k), idesc, acc);
+                for (int k = 0; k < KB_BYTES / 32; ++k) {
+                  const uint32_t acc = !first || k != 0;
+                  tc_mma<false>(dt, smem_desc(sw + 32 * k), smem_desc(st + 32 * k), idesc, acc);
+                  tc_mma<false>(dt + NS, smem_desc(sw + B_HALF + 32 * k), smem_desc(st + 32 * k), idesc, acc);
+                }
+                tc_commit(bar_empty(stage));
+                first = false;
               }
-              tc_commit(bar_empty(stage));
               if (++stage == YSTAGES) {
                 stage = 0;
                 phase ^= 1;
               }
-              if (kb == kblocks - 1) {
-                tc_commit(bar_tfull(buf));
-                if (++buf == 2) {
-                  buf = 0;
-                  tphase ^= 1;
-                }
-              }
+            }
+            if (!ok) break;
+            tc_commit(bar_tfull(buf));  // one of the two arrivals
+            if (++buf == 2) {
+              buf = 0;
+              tphase ^= 1;
             }
           }
           if (!ok) {
-            tc_commit(bar_drain);
-            mbar_drain(bar_drain, 0);
+            tc_commit(drain);
+            mbar_drain(drain, 0);
           }
         }
       } else if (warp >= 2 && warp < 2 + Y_EPI_WARPS) {
@@ -458,11 +480,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int row0 = seg_begin(cu_s, seg, mtok), row_end = seg_end(cu_s, seg, mtok);
           if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status, args.timeout_ns)) break;
           tc_fence_after();
-          const uint32_t tb = tmem_base + lane_addr + buf * (2 * NS);
+          const uint32_t tb = tmem_base + lane_addr + buf * (4 * NS);
           uint32_t d0[NS], d1[NS];
           tmem_ld32(tb, d0);
           tmem_ld32(tb + NS, d1);
           tmem_wait_ld();
+          {
+            uint32_t e[NS];
+            tmem_ld32(tb + 2 * NS, e);
+            tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < NS; ++n) d0[n] = __float_as_uint(__fadd_rn(__uint_as_float(d0[n]), __uint_as_float(e[n])));
+            tmem_ld32(tb + 3 * NS, e);
+            tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < NS; ++n) d1[n] = __float_as_uint(__fadd_rn(__uint_as_float(d1[n]), __uint_as_float(e[n])));
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(buf));

@@ -541,10 +541,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             sa = sbase + PairSmem::a + stage * A_BYTES;
             sb = sbase + PairSmem::b + stage * B_HALF;
           }
-          const uint32_t dt = tmem_base + buf * acc_cols;
+          // streaming pairs: even and odd K blocks accumulate apart (columns [2 NS b, +NS) and
+          // [2 NS b + NS, +NS)) and the epilogue adds the two sums, the order of the single-CTA
+          // kernel's two streaming lanes (k_dim % 128 == 0: an even K-block count)
+          const uint32_t dt = y_role ? tmem_base + buf * (2 * NS) + ((kb & 1) ? NS : 0) : tmem_base + buf * acc_cols;
+          const int kfirst = y_role ? (kb >> 1) : kb;
 #pragma unroll
           for (int k = 0; k < KB_BYTES / 32; ++k)
-            tc2_mma(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, (kb | k) != 0);
+            tc2_mma(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, (kfirst | k) != 0);
           tc2_commit(bar_empty(stage));
           tc2_commit(map_to(bar_empty(stage), peer));
           if (++stage == nst) {
@@ -646,8 +650,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (bar_red_or(2, 32 * Q_EPI_WARPS, !ok)) break;
       tc_fence_after();
       uint32_t d[NS];
-      tmem_ld32(tmem_base + lane_addr + buf * NS, d);
+      tmem_ld32(tmem_base + lane_addr + buf * (2 * NS), d);
       tmem_wait_ld();
+      {
+        uint32_t e[NS];
+        tmem_ld32(tmem_base + lane_addr + buf * (2 * NS) + NS, e);
+        tmem_wait_ld();
+#pragma unroll
+        for (int n = 0; n < NS; ++n) d[n] = __float_as_uint(__fadd_rn(__uint_as_float(d[n]), __uint_as_float(e[n])));
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -151,27 +151,26 @@ def streamed_counts(seed, n_big, big_rows, n_small):
 
 
 STREAM_CASES = [
-    # swiglu, layout, n (weight rows), big segments, their rows
-    (True, "contiguous", 4096, 9, 2000),      # 16 N-tiles
-    (False, "contiguous", 2048, 10, 3900),    # 8 N-tiles
-    (True, "batched", 4096, 12, 900),
-    (False, "batched", 2048, 34, 900),
-    (True, "contiguous", 2816, 10, 2100),     # 11 N-tiles: an odd N-tile count
-    (False, "contiguous", 2176, 10, 3000),    # 9 N-tiles, the last one half outside the weights
+    # swiglu, layout, n (weight rows), big segments, their rows, k
+    (True, "contiguous", 4096, 9, 2000, 256),      # 16 N-tiles
+    (False, "contiguous", 2048, 10, 3900, 256),    # 8 N-tiles
+    (True, "batched", 4096, 12, 900, 256),
+    (False, "batched", 2048, 34, 900, 256),
+    (True, "contiguous", 2816, 10, 2100, 256),     # 11 N-tiles: an odd N-tile count
+    (False, "contiguous", 2176, 10, 3000, 256),    # 9 N-tiles, the last one half outside the weights
 ]
 
 
 @pytest.mark.parametrize("pairs", [False, True], ids=["cta", "pairs"])
-@pytest.mark.parametrize("swiglu,layout,n,n_big,big_rows", STREAM_CASES,
-                         ids=[f"{'swiglu' if c[0] else 'plain'}-{c[1]}-n{c[2]}" for c in STREAM_CASES])
-def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_rows, pairs):
+@pytest.mark.parametrize("swiglu,layout,n,n_big,big_rows,k", STREAM_CASES,
+                         ids=[f"{'swiglu' if c[0] else 'plain'}-{c[1]}-n{c[2]}-k{c[5]}" for c in STREAM_CASES])
+def test_bf16_short_segments_on_streaming_ctas(swiglu, layout, n, n_big, big_rows, k, pairs):
     """Enough units per CTA that the launch splits its CTAs: segments of at most 32 rows go
     to streaming CTAs (weights as the MMA's M operand, the segment's rows as N = 32), the
     rest to the MMA pipeline.  Covers a short extra (shared-expert) segment, empty segments,
     row_scale on the plain epilogue, the batched layout's masked_m bounds, odd N-tile counts
     and a last N-tile that reaches past the weight rows."""
     need_gpu()
-    k = 256
     counts = streamed_counts(7 + swiglu + 2 * (layout == "batched") + n, n_big, big_rows, 60)
     counts.append(20)                   # the extra segment, short: streamed from w_extra
     num_w = len(counts) - 1
@@ -233,6 +232,27 @@ def test_pairs_and_single_cta_agree_bit_for_bit(swiglu):
     counts = streamed_counts(3, 12, 1500, 80)
     cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     g = torch.Generator().manual_seed(21)
+    a = torch.randn(int(cu[-1]), k, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(len(counts), n, k, generator=g) / k ** 0.5).to(torch.bfloat16).cuda()
+    epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE
+    cu_t = torch.from_numpy(cu).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, _ = moe.moe_grouped_gemm(a, cu_t, w, epilogue=epi, dev_status=st)
+    o2, _ = moe.moe_grouped_gemm(a, cu_t, w, epilogue=epi, dev_status=st, pairs=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+@pytest.mark.parametrize("swiglu,n,n_big,big_rows,k", [(True, 4096, 9, 2000, 256), (False, 2048, 10, 3900, 384)])
+def test_pairs_and_single_cta_agree_bit_for_bit_when_streaming(swiglu, n, n_big, big_rows, k):
+    """With segments of at most 32 rows on the streaming CTAs of both computations: the
+    streamed products are summed in the same order too (even and odd K blocks apart, then
+    added)."""
+    need_gpu()
+    counts = streamed_counts(31 + k, n_big, big_rows, 60)
+    cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    g = torch.Generator().manual_seed(23)
     a = torch.randn(int(cu[-1]), k, generator=g).to(torch.bfloat16).cuda()
     w = (torch.randn(len(counts), n, k, generator=g) / k ** 0.5).to(torch.bfloat16).cuda()
     epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE

@@ -1,10 +1,12 @@
 // BF16 grouped GEMM on CTA pairs with the 2-SM MMA (tcgen05.mma.cta_group::2), behind
 // moe_grouped_gemm_pairs.  It computes the same products in the same order as the
 // single-CTA kernel (gemm.cu), and its output is identical bit for bit.  Measured on GB300:
-// per SM its MMA pipeline runs a K step in 0.36 us against 0.40 us, but its streaming role
-// moves about half the bytes per SM, so on the prefill expert mix it is slower (gate/up 4.5
-// against 3.6 ms); on dense experts it ties or wins (down projection of 64 experts x 200
-// rows: 0.351 against 0.407 ms).  The layer uses the single-CTA kernel.
+// per SM its MMA pipeline runs a K step in 0.36 us against 0.40 us, but a streamed unit
+// costs its two SMs 1.7 times the SM time of a single streaming CTA, and a pair always
+// computes two M-tiles of one expert, so on the prefill expert mix it is slower (layer 6.29
+// against 5.99 ms per step on one box: gate/up 3.86 against 3.72 ms, down 2.00 against 1.82
+// ms); on dense experts it ties or wins (down projection of 64 experts x 200 rows: 0.351
+// against 0.407 ms).  The layer uses the single-CTA kernel.
 //
 // MoonEP page: the experts run as grouped matmuls (gate, up, down) over the cu_seqlens
 // segments.  This kernel computes them for BF16 operands on pairs of CTAs (clusters of two
@@ -22,7 +24,9 @@
 //     g and u side by side for its rows; plain: weight rows [256 nt + 128 r, +128) on rank r).
 //   Streaming pairs (segments of at most NS rows, when the launch has many units): the
 //     weights are the M operand (128 rows per CTA) and the segment's rows the N operand
-//     (N = NS, NS / 2 rows per CTA), through an 11-stage ring of 18 KB stages per CTA.  For
+//     (N = NS, NS / 2 rows per CTA), through a 10-stage ring of 18 KB stages per CTA run as
+//     two lanes (alternate K blocks, two TMA threads per CTA, two MMA threads in the
+//     leader, even and odd K blocks summed apart and then added).  For
 //     SwiGLU rank r holds gate rows [128 nt + 64 r, +64) and the matching up rows, so its
 //     tensor memory lanes 0-63 hold g and lanes 64-127 u of the same 64 output columns.
 //
@@ -49,11 +53,17 @@ namespace gg {
 
 constexpr int P_STAGES = 6;                          // MMA pipeline ring
 constexpr int P_STAGE_TX = A_BYTES + B_HALF;         // 32 KB per CTA per stage
-constexpr int Q_STAGES = 11;                         // streaming ring
+constexpr int Q_STAGES = 10;                         // streaming ring (even: two lanes own a parity each)
 constexpr int QT_ROWS = NS / 2;                      // token rows per CTA
 constexpr int QT_BYTES = QT_ROWS * KB_BYTES;         // 2 KB
 constexpr int Q_STAGE_BYTES = B_HALF + QT_BYTES;     // 18 KB, a multiple of 1024
 constexpr int Q_EPI_WARPS = 4;
+// Streaming pairs run two pipeline lanes, like the single-CTA kernel's streaming CTAs: lane p
+// (a TMA thread in each CTA, an MMA thread in the leader) takes the K blocks with
+// g % 2 == p of the pair's sequence, in the stages of parity p.  Lane 0 uses warps 0 and 1,
+// lane 1 the two warps after the streaming epilogue's.
+constexpr int Q_PRODUCER1 = 2 + Q_EPI_WARPS, Q_ISSUER1 = Q_PRODUCER1 + 1;
+static_assert(Q_ISSUER1 < THREADS / 32, "streaming warps");
 constexpr int Q_XPITCH = 17;                         // floats per lane row of the exchange (conflict-free)
 constexpr int NBAR_STAGES = Q_STAGES > P_STAGES ? Q_STAGES : P_STAGES;
 constexpr unsigned long long DRAIN_NS = 20000000ull;   // waits for work already in flight
@@ -76,9 +86,9 @@ struct PairSmem {
   static constexpr int q_xch = Q_STAGES * Q_STAGE_BYTES;
   static constexpr int y_end = q_xch + 2 * 2 * 32 * Q_XPITCH * 4;
   static constexpr int common_off = x_end > y_end ? x_end : y_end;
-  // common tail: barriers full[S], empty[S], tfull[2], tempty[2], drain; TMEM slot; abort
+  // common tail: barriers full[S], empty[S], tfull[2], tempty[2], drain[2]; TMEM slot; abort
   // flag; modelled role times; then int bnd[nseg + 1], prefix[nseg + 1], prefix_y[nseg + 1]
-  static constexpr int n_bars = 2 * NBAR_STAGES + 5;
+  static constexpr int n_bars = 2 * NBAR_STAGES + 6;
   static constexpr int tmem_slot = n_bars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int costs = abort_flag + 4;
@@ -94,9 +104,9 @@ static_assert(Q_STAGE_BYTES % 1024 == 0 && P_STAGE_TX % 1024 == 0, "swizzle atom
 // M-tiles of a segment with more than one M-tile, the single M-tile of a short segment on
 // the MMA pipeline (its 256 weight rows stream from HBM behind a shallow ring), and a
 // streamed segment.  They set how many pairs stream.  Measured per unit on the prefill
-// expert mix with both roles running (gate/up: about 40 us per pipeline unit, 47 us per
-// streamed unit).
-constexpr float COSTP_MMA = 40.0f, COSTP_SINGLE = 45.0f, COSTP_STREAM = 47.0f;
+// expert mix with both roles running (gate/up: about 41 us per pipeline unit, 31 us per
+// streamed unit on the two streaming lanes).
+constexpr float COSTP_MMA = 40.0f, COSTP_SINGLE = 45.0f, COSTP_STREAM = 31.0f;
 
 // ------------------------------------------------------------------ cluster / pair PTX
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -238,6 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar_tfull = [&](int b) { return smem_u32(bars + 2 * NBAR_STAGES + b); };
   auto bar_tempty = [&](int b) { return smem_u32(bars + 2 * NBAR_STAGES + 2 + b); };
   const uint32_t bar_drain = smem_u32(bars + 2 * NBAR_STAGES + 4);
+  const uint32_t bar_drain1 = smem_u32(bars + 2 * NBAR_STAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cmn + PairSmem::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cmn + PairSmem::abort_flag);
   float* costs = reinterpret_cast<float*>(cmn + PairSmem::costs);
@@ -352,10 +363,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tfull(b), y_role ? 2 : 1);                            // streaming: one per lane
       mbar_init(bar_tempty(b), 2 * (y_role ? Q_EPI_WARPS : EPI_WARPS));   // both CTAs' epilogue warps
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain1, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -402,13 +414,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int u_step = y_role ? nyp : gxu;
   const int mgroup = SWIGLU ? MGROUP_GATE_UP / 2 : 0;
 
-  if (warp == 0) {
+  if (warp == 0 || (y_role && warp == Q_PRODUCER1)) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
+    // (streaming: lane p = 0, 1 fills the stages of parity p)
     if (lane == 0) {
+      const uint32_t lp = warp == 0 ? 0u : 1u;
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
       int stage = 0;
-      uint32_t phase = 0, armed = 0, last_parity = 0;
+      uint32_t phase = 0, armed = 0, last_parity = 0, g = 0;
       bool ok = true;
       uint64_t wpol;
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(wpol));
@@ -445,7 +459,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             n1 = SWIGLU ? n0 + args.n_dim / 2 : -1;
           }
         }
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < kblocks; ++kb, ++g) {
+          if (y_role && (g & 1u) != lp) {   // the other lane's K block
+            if (++stage == nst) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if (y_role) {
             const int pk = kb + STREAM_PREFETCH_KB;
             if (pk < kblocks) {
@@ -511,22 +532,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (armed & (1u << s)) pdrain(bar_empty(s), (last_parity >> s) & 1u);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (y_role && warp == Q_ISSUER1)) {
     if (lane == 0 && leader) {
-      // ---------------------------------------------------------- MMA issuer (leader)
+      // ---------------------------------------------------------- MMA issuer (leader; streaming:
+      // lane p = 0, 1 consumes the stages of parity p)
+      const uint32_t lp = warp == 1 ? 0u : 1u;
+      const uint32_t drain = lp == 0 ? bar_drain : bar_drain1;
       const uint32_t idesc = instr_desc_pair(y_role ? NS : BN);
       const int acc_cols = y_role ? NS : BN;
       int stage = 0, buf = 0;
-      uint32_t phase = 0, tphase = 0;
+      uint32_t phase = 0, tphase = 0, g = 0;
       bool ok = true;
       for (int u = u_first; ok && u < u_end; u += u_step) {
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < kblocks; ++kb, ++g) {
           if (kb == 0) {
             if (!pwait<true>(bar_tempty(buf), tphase ^ 1, ab)) {
               ok = false;
               break;
             }
             tc_fence_after();
+          }
+          if (y_role && (g & 1u) != lp) {   // the other lane's K block
+            if (++stage == nst) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
           }
           if (!pwait<false>(bar_full(stage), phase, ab)) {
             ok = false;
@@ -555,19 +586,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1;
           }
-          if (kb == kblocks - 1) {
-            tc2_commit(bar_tfull(buf));
-            tc2_commit(map_to(bar_tfull(buf), peer));
-            if (++buf == 2) {
-              buf = 0;
-              tphase ^= 1;
-            }
-          }
+        }
+        if (!ok) break;
+        tc2_commit(bar_tfull(buf));   // streaming: one of the two arrivals
+        tc2_commit(map_to(bar_tfull(buf), peer));
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1;
         }
       }
       if (!ok) {
-        tc2_commit(bar_drain);  // arrives once every MMA issued so far has completed
-        pdrain(bar_drain, 0);
+        tc2_commit(drain);  // arrives once every MMA this thread issued has completed
+        pdrain(drain, 0);
       }
     }
   } else if (!y_role) {

@@ -90,3 +90,40 @@ def test_wait_that_runs_out_aborts_cleanly(kind, swiglu):
     assert torch.equal(out2.view(torch.uint8), ref_out.view(torch.uint8))
     if ref_s is not None:
         assert torch.equal(out2_s, ref_s)
+
+
+@pytest.mark.parametrize("pairs", [False, True], ids=["cta", "pairs"])
+@pytest.mark.parametrize("swiglu", [False, True], ids=["plain", "swiglu"])
+def test_wait_that_runs_out_aborts_cleanly_with_streaming(swiglu, pairs):
+    """The same on a launch large enough to split its CTAs: segments of at most 32 rows on
+    the streaming CTAs, whose two pipeline lanes (two TMA threads, two MMA threads) each
+    drain their own stages and MMAs on the way out."""
+    need_gpu()
+    f = wait_limit_fn()
+    rng = np.random.default_rng(41 + swiglu + 2 * pairs)
+    counts = list(rng.integers(0, 33, 60)) + [3900 + int(rng.integers(0, 100)) for _ in range(10)]
+    rng.shuffle(counts)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32)
+    k, n, E = 256, 2048, len(counts)
+    g = torch.Generator().manual_seed(43)
+    a = torch.randn(int(cu[-1]), k, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(E, n, k, generator=g) / k ** 0.5).to(torch.bfloat16).cuda()
+    cols = n // 2 if swiglu else n
+    epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE
+    mk = lambda: torch.zeros(a.shape[0], cols, dtype=torch.bfloat16, device="cuda")
+    cu_d = cu.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref_out = mk()
+    run(f, a, None, cu_d, w, None, moe.MOE_BF16, epi, ref_out, None, st, 2_000_000_000, pairs)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    out = mk()
+    run(f, a, None, cu_d, w, None, moe.MOE_BF16, epi, out, None, st, 4, pairs)
+    torch.cuda.synchronize()       # the call returned: nothing waits forever
+    assert st.item() & moe.MOE_DEV_PIPELINE_TIMEOUT
+    st.zero_()
+    out2 = mk()
+    run(f, a, None, cu_d, w, None, moe.MOE_BF16, epi, out2, None, st, 2_000_000_000, pairs)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(out2.view(torch.int16), ref_out.view(torch.int16))

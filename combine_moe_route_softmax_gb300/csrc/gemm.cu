@@ -85,12 +85,14 @@ static_assert(SmemLayout::costs + 8 <= SmemLayout::arrays, "common tail header")
 static_assert(STAGES <= YSTAGES, "barrier slots");
 // Relative time of one unit (all units of a launch have the same K): an MMA-bound tile, a
 // single-tile segment's tile on the MMA pipeline, and a streamed unit.  They set how many
-// CTAs stream; measured per unit on the prefill expert mix with both roles running (gate/up:
-// 45.4 and 50.7 us; down: 12.9 and 14.8 us), the streamed cost rounded up so that the
-// streaming CTAs, which cannot hand work back, are not the last to finish.
+// CTAs stream.  Measured per unit on the prefill expert mix with both roles running: an
+// MMA-pipeline unit 45-48 us on gate/up and 13 us on down, a streamed unit (two lanes) 37
+// and 11 us; the streamed cost is set above that (24 streaming CTAs of 152 instead of 20),
+// which timed best: a faster streaming role takes L2 and HBM bandwidth from the pipeline.
 constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 42.0f;
-// Streaming CTAs: warp 0 loads the ring, warp 1 issues the MMAs, warps 2..5 are the
-// epilogue (one unit streams for tens of microseconds; its epilogue is short).
+// Streaming CTAs: warps 0 and Y_PRODUCER1 load the ring, warps 1 and Y_ISSUER1 issue the
+// MMAs (one pair per pipeline lane), warps 2..5 are the epilogue (one unit streams for tens
+// of microseconds; its epilogue is short).
 constexpr int Y_EPI_WARPS = 4;
 constexpr int Y_PRODUCER1 = 2 + Y_EPI_WARPS, Y_ISSUER1 = Y_PRODUCER1 + 1;  // lane 1 of the streaming pipeline
 static_assert(Y_ISSUER1 < THREADS / 32, "streaming warps");

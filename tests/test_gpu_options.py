@@ -172,14 +172,17 @@ def test_dispatch_fake_quant_rejected_for_e4m3_layers():
     assert e.value.code == 3
 
 
+@pytest.mark.parametrize("full", [False, True], ids=["reduced", "full"])
 @pytest.mark.parametrize("weight_in_down", [False, True])
-def test_layer_gemm_pairs_bit_identical(weight_in_down):
+def test_layer_gemm_pairs_bit_identical(weight_in_down, full):
     """gemm_pairs runs both grouped GEMMs on SM pairs: the layer output equals the default
-    layer's bit for bit (prefill shapes, reduced, with the shared expert and the skewed
-    routing that gives long and short segments); E4M3, the batched layout and the fused
-    combine are refused."""
+    layer's bit for bit (prefill shapes, reduced and full size, with the shared expert and the
+    skewed routing that gives long and short segments; at full size both computations run
+    streaming CTAs); E4M3, the batched layout and the fused combine are refused."""
     need_gpu()
-    w = scaled(WORKLOADS["prefill"], T=1024, T_valid=768, E=32)
+    if full and weight_in_down:
+        pytest.skip("one full-size case is enough")
+    w = WORKLOADS["prefill"] if full else scaled(WORKLOADS["prefill"], T=1024, T_valid=768, E=32)
     logits = synth.router_logits(w, 0, device="cuda")
     x = synth.hidden(w, 0, device="cuda")
     w13, w2, s13, s2 = synth.expert_weights(w, 0, device="cuda")

@@ -18,9 +18,9 @@
 // the grid, BF16 and not fused, when the launch has at least 16 units per CTA) take the
 // segments of at most NS rows: such a segment is a weight stream, so its CTAs keep six
 // 32 KB weight tiles in flight behind 4 KB token tiles and issue MMAs with the weights as
-// the M = 128 operand and the segment's rows as N = NS, on two pipeline lanes (two TMA
-// threads, two MMA threads, alternate K blocks).  Every CTA derives the same ny from the
-// segment lengths and a per-unit cost model, so no host sync is needed.
+// the M = 128 operand and the segment's rows as N = NS, on one pipeline lane (gate/up) or
+// two (down: two TMA threads, two MMA threads, alternate K blocks).  Every CTA derives the
+// same ny from the segment lengths and a per-unit cost model, so no host sync is needed.
 //
 // Warp roles of the MMA pipeline (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane)
@@ -36,7 +36,8 @@
 //         float32 per 128 elements rather than a format the MMA applies itself.
 //
 // Warp roles of a streaming CTA: warps 0 and 6 TMA producers of pipeline lanes 0 and 1,
-// warps 1 and 7 their MMA issuers (warp 1 also allocates TMEM), warps 2..5 epilogue.
+// warps 1 and 7 their MMA issuers (warp 1 also allocates TMEM), warps 2..5 epilogue; with
+// one lane, warps 6 and 7 idle.
 //
 // Every mbarrier wait is bounded (about 2 s of globaltimer); on expiry the CTA sets
 // MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producers
@@ -83,13 +84,21 @@ struct SmemLayout {
 };
 static_assert(SmemLayout::costs + 8 <= SmemLayout::arrays, "common tail header");
 static_assert(STAGES <= YSTAGES, "barrier slots");
+// Streaming pipeline lanes per GEMM: the down projection streams on two lanes, gate/up on
+// one.  Two lanes make a streamed unit 1.5 times faster, but the faster weight stream takes
+// L2 and HBM bandwidth from the MMA pipeline, whose gate/up units (3.7 MB of weights per
+// N-tile) lose more than the streaming role gains: in same-box A/B runs gate/up was 1.4 %
+// faster on one lane, down 1.5 % faster on two.
+template <bool SWIGLU>
+__host__ __device__ constexpr int y_lanes() { return SWIGLU ? 1 : 2; }
 // Relative time of one unit (all units of a launch have the same K): an MMA-bound tile, a
 // single-tile segment's tile on the MMA pipeline, and a streamed unit.  They set how many
 // CTAs stream.  Measured per unit on the prefill expert mix with both roles running: an
-// MMA-pipeline unit 45-48 us on gate/up and 13 us on down, a streamed unit (two lanes) 37
-// and 11 us; the streamed cost is set above that (24 streaming CTAs of 152 instead of 20),
-// which timed best: a faster streaming role takes L2 and HBM bandwidth from the pipeline.
-constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 42.0f;
+// MMA-pipeline unit about 45 us on gate/up and 13 us on down, a streamed unit 50.7 us on one
+// lane (gate/up) and 11 us on two (down); each streamed cost is set above its measurement
+// so that the streaming CTAs, which cannot hand work back, do not finish last (with two
+// lanes, 24 streaming CTAs of 152 timed best).
+constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM_1LANE = 53.5f, COST_STREAM_2LANES = 42.0f;
 // Streaming CTAs: warps 0 and Y_PRODUCER1 load the ring, warps 1 and Y_ISSUER1 issue the
 // MMAs (one pair per pipeline lane), warps 2..5 are the epilogue (one unit streams for tens
 // of microseconds; its epilogue is short).
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int l = len(s);
       if (streamed(l)) {
         ++local_y;
-        cy += COST_STREAM;
+        cy += y_lanes<SWIGLU>() == 2 ? COST_STREAM_2LANES : COST_STREAM_1LANE;
       } else {
         const int m = (l + BM - 1) / BM;
         local += m;
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_tfull(b), y_role ? 2 : 1);   // streaming: one arrival per pipeline lane
+      mbar_init(bar_tfull(b), y_role ? y_lanes<SWIGLU>() : 1);   // streaming: one arrival per lane
       mbar_init(bar_tempty(b), y_role ? Y_EPI_WARPS : EPI_WARPS);
     }
     mbar_init(bar_drain, 1);
@@ -345,10 +354,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Unit v: the t-th streamed segment (t = v / n_tiles) and N-tile nt = v % n_tiles.  The
       // two 128-row halves of the weight tile are the A operands of two MMAs (M = 128) that
       // share the segment's NS token rows as B (N = NS).
-      // The K blocks of this CTA's units, numbered g = 0, 1, ... in order, run on two lanes
-      // of the pipeline: lane p (producer thread p, MMA thread p) takes the K blocks with
-      // g % 2 == p, which live in the stages of parity p (stage g % YSTAGES, YSTAGES even),
-      // and accumulates into its own TMEM columns; the epilogue adds lane 0's sum (even K
+      // The K blocks of this CTA's units, numbered g = 0, 1, ... in order, run on kLanes
+      // lanes of the pipeline (y_lanes: two for the down projection, one for gate/up): lane p
+      // (producer thread p, MMA thread p) takes the K blocks with g % kLanes == p, which with
+      // two lanes live in the stages of parity p (stage g % YSTAGES, YSTAGES even), and
+      // accumulates into its own TMEM columns; the epilogue adds lane 0's sum (even K
       // blocks) and lane 1's (odd K blocks), in that order.  k_dim is a multiple of 128, so
       // a unit has an even number of 64-wide K blocks and g % 2 == kb % 2.  A single MMA
       // thread waits on a barrier between every two groups of eight short MMAs and the
@@ -368,7 +378,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         seg = lo;
       };
-      if (warp == 0 || warp == Y_PRODUCER1) {
+      constexpr int kLanes = y_lanes<SWIGLU>();
+      if (warp == 0 || (kLanes == 2 && warp == Y_PRODUCER1)) {
         const uint32_t p = warp == 0 ? 0u : 1u;
         if (lane == 0) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmAt)) : "memory");
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int rA = SWIGLU ? wbase + nt * 128 : wbase + nt * BN;
             const int rB = SWIGLU ? wbase + args.n_dim / 2 + nt * 128 : rA + 128;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
-              if ((g & 1u) == p) {
+              if (g % static_cast<uint32_t>(kLanes) == p) {
                 if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
                   ok = false;
                   break;
@@ -417,7 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
           }
         }
-      } else if (warp == 1 || warp == Y_ISSUER1) {
+      } else if (warp == 1 || (kLanes == 2 && warp == Y_ISSUER1)) {
         const uint32_t p = warp == 1 ? 0u : 1u;
         if (lane == 0) {
           constexpr uint32_t idesc = instr_desc_stream();
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t dt = tmem_base + buf * (4 * NS) + p * (2 * NS);
             bool first = true;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
-              if ((g & 1u) == p) {
+              if (g % static_cast<uint32_t>(kLanes) == p) {
                 if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
                   ok = false;
                   break;
@@ -487,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tb, d0);
           tmem_ld32(tb + NS, d1);
           tmem_wait_ld();
-          {
+          if (kLanes == 2) {
             uint32_t e[NS];
             tmem_ld32(tb + 2 * NS, e);
             tmem_wait_ld();

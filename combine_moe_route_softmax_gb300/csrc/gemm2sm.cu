@@ -14,8 +14,10 @@
 // shared memory and half of the N rows of B, and each CTA's tensor memory receives its own
 // 128 rows of the product.  Per 64-wide K step a CTA therefore fills 32 KB of shared memory
 // (16 KB of A, 16 KB of B) for 128 x 256 products, where a CTA working alone fills 48 KB
-// for the same work; the fill rate of one SM from L2, not the tensor core, is what bounds
-// the single-CTA tile.  No copy is multicast: every CTA loads only its own tiles.
+// for the same work; on the prefill mix the single-CTA tile's tensor pipe waits about a
+// fifth of its cycles for operand tiles coming from L2, and a third fewer bytes per step
+// recovers about a tenth of the time.  No copy is multicast: every CTA loads only its own
+// tiles.
 //
 // Two roles, both on pairs.
 //   MMA pipeline (segments of more than NS rows): a unit is two M-tiles of one segment

@@ -50,6 +50,17 @@ namespace gg {
 
 constexpr int STAGES = 4;
 constexpr int STAGE_TX = A_BYTES + B_BYTES;
+// BF16 gate/up (not fused): an MMA-pipeline unit is two M-tiles of one segment sharing each
+// weight tile (256 x 256 outputs, both 256-column accumulators in TMEM), so a K step moves
+// 64 KB (two A tiles and one weight tile) for twice the work of a 48 KB single-tile step:
+// a third fewer operand bytes per product, on a path whose tensor pipe waits about a fifth
+// of its cycles for operand tiles.  Three 64 KB stages fill the same shared memory as four
+// 48 KB ones.  The accumulators are not double-buffered; the epilogue frees the first one
+// as soon as it has read it, and the next unit's MMAs into it start then (a single buffer
+// cost 0.2-0.6 % on the one-tile path).
+constexpr int STAGES_M2 = 3;
+constexpr int STAGE_M2_BYTES = 2 * A_BYTES + B_BYTES;   // 64 KB
+static_assert(STAGES_M2 * STAGE_M2_BYTES == STAGES * (A_BYTES + B_BYTES), "same shared memory as the one-tile ring");
 
 // Streamed segments (BF16, not fused): a segment of at most NS rows is computed by a
 // streaming CTA with the weights as the MMA's M operand (two M = 128 halves of a 256-row
@@ -99,6 +110,8 @@ __host__ __device__ constexpr int y_lanes() { return SWIGLU ? 1 : 2; }
 // so that the streaming CTAs, which cannot hand work back, do not finish last (with two
 // lanes, 24 streaming CTAs of 152 timed best).
 constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM_1LANE = 53.5f, COST_STREAM_2LANES = 42.0f;
+// two-tile unit of the gate/up pipeline (relative to COST_MMA per single tile)
+constexpr float COST_MMA2 = 84.0f;
 // Streaming CTAs: warps 0 and Y_PRODUCER1 load the ring, warps 1 and Y_ISSUER1 issue the
 // MMAs (one pair per pipeline lane), warps 2..5 are the epilogue (one unit streams for tens
 // of microseconds; its epilogue is short).
@@ -192,6 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr bool M2 = SWIGLU && !FP8 && !FUSE;   // two M-tiles per MMA-pipeline unit
   uint8_t* cmn = smem + args.common_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(cmn);
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
@@ -244,8 +258,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         cy += y_lanes<SWIGLU>() == 2 ? COST_STREAM_2LANES : COST_STREAM_1LANE;
       } else {
         const int m = (l + BM - 1) / BM;
-        local += m;
-        cx += m == 1 ? COST_SINGLE : COST_MMA * static_cast<float>(m);
+        local += M2 ? (m + 1) / 2 : m;
+        cx += m == 1 ? COST_SINGLE
+                     : (M2 ? COST_MMA2 * static_cast<float>(m / 2) + static_cast<float>(m & 1) * COST_MMA
+                           : COST_MMA * static_cast<float>(m));
       }
     }
     int incl = local, incl_y = local_y;
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (streamed(l))
         ++run_y;
       else
-        run += (l + BM - 1) / BM;
+        run += M2 ? ((l + BM - 1) / BM + 1) / 2 : (l + BM - 1) / BM;
     }
     if (lane == 31) {
       prefix[nseg] = incl;
@@ -285,6 +301,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   const int total_units = prefix[nseg] * n_tiles;
   const int total_y = prefix_y[nseg] * n_tiles;
+  // MMA-pipeline unit u -> segment, N-tile, first row (two-tile units: the prefix counts
+  // pairs of M-tiles, so the decoder's row0 is the segment start + (pair index) * BM)
+  auto mma_unit = [&](int u) {
+    Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok,
+                         M2 ? MGROUP_GATE_UP / 2 : (SWIGLU && !FP8 ? MGROUP_GATE_UP : 0));
+    if (M2) {
+      const int b0 = seg_begin(cu_s, w.seg, mtok);
+      w.row0 = b0 + 2 * (w.row0 - b0);
+    }
+    return w;
+  };
   // CTAs [gx, gridDim.x) stream; every CTA derives the same split from the same counts.
   int ny = 0;
   if (total_y > 0) {
@@ -309,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     gxu = min(gx, (total_units + per - 1) / per);
   }
   if (tid == 64) {
-    const int nst = y_role ? YSTAGES : STAGES;
+    const int nst = y_role ? YSTAGES : (M2 ? STAGES_M2 : STAGES);
     for (int s = 0; s < nst; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
@@ -555,26 +582,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t last_parity = 0;  // bit s: parity of the last phase armed on stage s
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
-        const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok, SWIGLU && !FP8 ? MGROUP_GATE_UP : 0);
+        const Unit w = mma_unit(u);
         const bool extra = w.seg >= args.num_w;
         const CUtensorMap* mb = extra ? &tmBx : &tmB;
         const int wbase = extra ? 0 : w.seg * args.n_dim;
         const int rA = SWIGLU ? wbase + w.nt * 128 : wbase + w.nt * BN;
         const int rB = SWIGLU ? wbase + args.n_dim / 2 + w.nt * 128 : rA + 128;
+        // two-tile units: the second M-tile's rows when the segment has them
+        const bool two = M2 && w.row0 + BM < w.row_end;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(bar_empty(stage), phase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(bar_full(stage), STAGE_TX);
+          mbar_expect_tx(bar_full(stage), M2 ? (two ? STAGE_M2_BYTES : STAGE_M2_BYTES - A_BYTES) : STAGE_TX);
           armed |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
-          const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
-          tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
-          tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
-          tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
-          if (++stage == STAGES) {
+          if (M2) {
+            // stage: [A rows of M-tile 0 | A rows of M-tile 1 | 256 weight rows]
+            const uint32_t sa = sbase + stage * STAGE_M2_BYTES;
+            const uint32_t sb = sa + 2 * A_BYTES;
+            tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
+            if (two) tma_load_2d(sa + A_BYTES, &tmA, kb * KE, w.row0 + BM, bar_full(stage));
+            tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
+            tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
+          } else {
+            const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
+            const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
+            tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
+            tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
+            tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
+          }
+          if (++stage == (M2 ? STAGES_M2 : STAGES)) {
             stage = 0;
             phase ^= 1;
           }
@@ -582,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) {
         // wait for the copies this CTA still has in flight before its shared memory goes away
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < (M2 ? STAGES_M2 : STAGES); ++s)
           if (armed & (1u << s)) mbar_drain(bar_full(s), (last_parity >> s) & 1u);
       }
     }
@@ -595,40 +634,91 @@ __global__ void __launch_bounds__(THREADS, 1)
       int buf = 0;
       uint32_t tphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
-        for (int kb = 0; kb < kblocks; ++kb) {
-          const bool round_start = FP8 || kb == 0;
-          if (round_start) {
-            if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+      if constexpr (M2) {
+        // two-tile units: accumulator t (TMEM columns [BN t, +BN)) holds M-tile t, one buffer.
+        // At a unit's first K step the MMAs into accumulator 0 wait for the epilogue to have
+        // read it, those into accumulator 1 for the second read, so the epilogue's work on
+        // M-tile 0 overlaps the new unit's first MMAs.
+        for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
+          const Unit w = mma_unit(u);
+          const bool two = w.row0 + BM < w.row_end;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (kb == 0) {
+              if (!mbar_wait(bar_tempty(0), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-          }
-          if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
-          const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
-          const uint32_t dt = tmem_base + buf * BN;
+            const uint32_t sa = sbase + stage * STAGE_M2_BYTES;
+            const uint32_t sb = sa + 2 * A_BYTES;
 #pragma unroll
-          for (int k = 0; k < KB_BYTES / 32; ++k) {
-            const uint32_t acc = (FP8 ? k : (kb | k)) != 0;
-            tc_mma<FP8>(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, acc);
+            for (int k = 0; k < KB_BYTES / 32; ++k)
+              tc_mma<false>(tmem_base, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, (kb | k) != 0);
+            if (kb == 0) {
+              if (!mbar_wait(bar_tempty(1), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (two) {
+#pragma unroll
+              for (int k = 0; k < KB_BYTES / 32; ++k)
+                tc_mma<false>(tmem_base + BN, smem_desc(sa + A_BYTES + 32 * k), smem_desc(sb + 32 * k), idesc,
+                              (kb | k) != 0);
+            }
+            tc_commit(bar_empty(stage));
+            if (++stage == STAGES_M2) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          tc_commit(bar_empty(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-          const bool round_end = FP8 || kb == kblocks - 1;
-          if (round_end) {
-            tc_commit(bar_tfull(buf));
-            if (++buf == 2) {
-              buf = 0;
-              tphase ^= 1;
+          if (!ok) break;
+          tc_commit(bar_tfull(0));
+          tphase ^= 1;
+        }
+      } else {
+        for (int u = blockIdx.x; ok && u < total_units; u += gxu) {
+          for (int kb = 0; kb < kblocks; ++kb) {
+            const bool round_start = FP8 || kb == 0;
+            if (round_start) {
+              if (!mbar_wait(bar_tempty(buf), tphase ^ 1, abort_flag, args.dev_status, args.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (!mbar_wait(bar_full(stage), phase, abort_flag, args.dev_status, args.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
+            const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
+            const uint32_t dt = tmem_base + buf * BN;
+#pragma unroll
+            for (int k = 0; k < KB_BYTES / 32; ++k) {
+              const uint32_t acc = (FP8 ? k : (kb | k)) != 0;
+              tc_mma<FP8>(dt, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), idesc, acc);
+            }
+            tc_commit(bar_empty(stage));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            const bool round_end = FP8 || kb == kblocks - 1;
+            if (round_end) {
+              tc_commit(bar_tfull(buf));
+              if (++buf == 2) {
+                buf = 0;
+                tphase ^= 1;
+              }
             }
           }
         }
@@ -653,170 +743,212 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int active = min(gxu, total_units);
       zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
     }
-    for (int u = blockIdx.x; u < total_units; u += gxu) {
-      const Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok, SWIGLU && !FP8 ? MGROUP_GATE_UP : 0);
-      const int row = w.row0 + r_in_tile;
-      const bool row_ok = row < w.row_end;
-      // first output column this thread covers and whether that 128-column block exists
-      const int col0 = SWIGLU ? w.nt * 128 + 64 * half : w.nt * BN + 128 * half;
-      const bool cols_ok = col0 < out_cols;
-      float acc[128];
-      if (FP8) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-      }
-      const bool extra = w.seg >= args.num_w;
-      // FP8: a warp whose 32 rows all lie past the segment's end has nothing to promote in
-      // any of the K rounds and only keeps the TMEM hand-off going (decode segments often
-      // hold a few rows).  BF16 has one round per tile and keeps the plain path.
-      const bool warp_live = !FP8 || w.row0 + 32 * q < w.row_end;
-      int rounds = FP8 ? kbs_total : 1;
-      bool ok = true;
-      // FP8 weight scales of this unit: one row of K-block scales for each 128 weight rows
-      const float* wsc = nullptr;
-      size_t ws0 = 0, ws1 = 0;
-      if (FP8) {
-        wsc = extra ? args.wx_scales : args.w_scales + (size_t)w.seg * (args.n_dim / 128) * kbs_total;
-        if (SWIGLU) {
-          ws0 = (size_t)w.nt * kbs_total;                            // gate rows
-          ws1 = (size_t)(args.n_dim / 256 + w.nt) * kbs_total;       // up rows
-        } else {
-          ws0 = ws1 = (size_t)((w.nt * BN + 128 * half) / 128) * kbs_total;
-        }
-      }
-      for (int rd = 0; rd < rounds; ++rd) {
-        if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status, args.timeout_ns)) {
-          ok = false;
-          break;
-        }
+    if constexpr (M2) {
+      // two-tile units (BF16 gate/up): read accumulator 0, free it, compute and store M-tile
+      // 0's h; then accumulator 1 (freed at once when the unit has one M-tile) and M-tile 1
+      for (int u = blockIdx.x; u < total_units; u += gxu) {
+        const Unit w = mma_unit(u);
+        const bool two = w.row0 + BM < w.row_end;
+        const int col0 = w.nt * 128 + 64 * half;
+        const bool cols_ok = col0 < out_cols;
+        if (!mbar_wait(bar_tfull(0), tphase, abort_flag, args.dev_status, args.timeout_ns)) break;
         tc_fence_after();
-        const uint32_t tb = tmem_base + lane_addr + buf * BN;
-        if (!warp_live) {
-          // nothing to read
-        } else if (FP8) {
-          // promotion of this K block: acc += partial * (s_a[row, kb] * s_w[block, kb])
-          const float sa = row_ok ? args.a_scales[(size_t)row * kbs_total + rd] : 0.0f;
-          const float s0 = cols_ok ? wsc[ws0 + rd] * sa : 0.0f;
-          const float s1 = cols_ok ? wsc[ws1 + rd] * sa : 0.0f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
-                                    : 128 * half + 32 * c;
-            uint32_t r[32];
-            tmem_ld32(tb + tcol, r);
-            tmem_wait_ld();
-            const float sc = (SWIGLU && c >= 2) ? s1 : s0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * c + i]);
+        for (int t = 0; t < 2; ++t) {
+          if (t == 1 && !two) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty(1));
+            break;
           }
-        } else {
+          float acc[128];
+          const uint32_t tb = tmem_base + lane_addr + t * BN;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
-                                    : 128 * half + 32 * c;
+            const int tcol = c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2);
             uint32_t r[32];
             tmem_ld32(tb + tcol, r);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[32 * c + i] = __uint_as_float(r[i]);
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(buf));
-        if (++buf == 2) {
-          buf = 0;
-          tphase ^= 1;
-        }
-      }
-      // FP8 SwiGLU: the eight warps exchange row maxima through a named barrier below, so
-      // they agree on leaving (one reduction per unit on every warp) before any of them does
-      if (FP8 && SWIGLU) {
-        if (bar_red_or(1, 32 * EPI_WARPS, !ok)) break;
-      } else if (!ok) {
-        break;
-      }
-      // ---- tile epilogue from registers
-      if (SWIGLU) {
-        float h[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
-        if (!FP8) {
-          if (row_ok && cols_ok) store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
-        } else {
-          // 1x128 block of h = this thread's 64 columns + the partner half's 64
-          float amax = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(h[i]));
-          xch[half * 128 + r_in_tile] = amax;
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          amax = fmaxf(amax, xch[(1 - half) * 128 + r_in_tile]);
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          const float s = block_scale(amax);
-          if (row_ok && cols_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + (size_t)row * out_cols + col0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t o[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) word |= (uint32_t)f32_to_e4m3(__fdiv_rn(h[16 * v + 4 * j + b], s)) << (8 * b);
-                o[j] = word;
-              }
-              dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            if (half == 0) args.out_scales[(size_t)row * (out_cols / 128) + w.nt] = s;
-          }
-        }
-      } else if (cols_ok) {
-        if (args.row_scale) {
-          // router weight of each permuted row, applied to the float32 accumulator
-          const float rs = row_ok ? args.row_scale[row] : 0.0f;
-#pragma unroll
-          for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
-        }
-        const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
-        store_rows_bf16(acc, stage_out + (warp - 2) * STAGE_OUT_BYTES, lane, rows_here,
-                        static_cast<uint16_t*>(args.out), w.row0 + 32 * q, out_cols, col0);
-        if (FUSE) {
-          // Rows [row0 + 32q, + rows_here) x columns [col0, col0 + 128) are stored.  Each lane
-          // counts its row in the (token, 128-column block) counter; the lane whose count
-          // completes the token's rows (its valid slots + its shared row) has its warp sum
-          // the block.  Every lane's stores are fenced before the counts (release); the
-          // summing warp fences again before it reads the rows (acquire).  No CTA waits.
-          __threadfence();
+          tc_fence_before();
           __syncwarp();
-          int done_t = -1;
-          if (lane < rows_here) {
-            const int src = args.src_row[w.row0 + 32 * q + lane];
-            const int TK = args.T * args.K;
-            const int t = src < TK ? src / args.K : src - TK;
-            if (src >= 0 && t < args.T) {
-              // rows of token t: its valid slots and its shared row (loads issued together)
-              int target = 0;
-              for (int k0 = 0; k0 < args.K; k0 += 8) {
-                int pv[8];
+          if (lane == 0) mbar_arrive(bar_tempty(t));
+          const int row = w.row0 + t * BM + r_in_tile;
+          if (row < w.row_end && cols_ok) {
+            float h[64];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) pv[j] = k0 + j < args.K ? args.inv_map[(size_t)t * args.K + k0 + j] : -1;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) target += pv[j] >= 0;
-              }
-              if (args.shared_map && args.shared_map[t] >= 0) ++target;
-              int32_t* cnt = args.counters + (size_t)t * (args.n_dim / 128) + col0 / 128;
-              if (atomicAdd(cnt, 1) == target - 1) {
-                *cnt = 0;   // every row of this block has arrived: reset for the next call
-                done_t = t;
-              }
+            for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
+            store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+          }
+        }
+        tphase ^= 1;
+      }
+    } else {
+      for (int u = blockIdx.x; u < total_units; u += gxu) {
+        const Unit w = mma_unit(u);
+        const int row = w.row0 + r_in_tile;
+        const bool row_ok = row < w.row_end;
+        // first output column this thread covers and whether that 128-column block exists
+        const int col0 = SWIGLU ? w.nt * 128 + 64 * half : w.nt * BN + 128 * half;
+        const bool cols_ok = col0 < out_cols;
+        float acc[128];
+        if (FP8) {
+  #pragma unroll
+          for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        }
+        const bool extra = w.seg >= args.num_w;
+        // FP8: a warp whose 32 rows all lie past the segment's end has nothing to promote in
+        // any of the K rounds and only keeps the TMEM hand-off going (decode segments often
+        // hold a few rows).  BF16 has one round per tile and keeps the plain path.
+        const bool warp_live = !FP8 || w.row0 + 32 * q < w.row_end;
+        int rounds = FP8 ? kbs_total : 1;
+        bool ok = true;
+        // FP8 weight scales of this unit: one row of K-block scales for each 128 weight rows
+        const float* wsc = nullptr;
+        size_t ws0 = 0, ws1 = 0;
+        if (FP8) {
+          wsc = extra ? args.wx_scales : args.w_scales + (size_t)w.seg * (args.n_dim / 128) * kbs_total;
+          if (SWIGLU) {
+            ws0 = (size_t)w.nt * kbs_total;                            // gate rows
+            ws1 = (size_t)(args.n_dim / 256 + w.nt) * kbs_total;       // up rows
+          } else {
+            ws0 = ws1 = (size_t)((w.nt * BN + 128 * half) / 128) * kbs_total;
+          }
+        }
+        for (int rd = 0; rd < rounds; ++rd) {
+          if (!mbar_wait(bar_tfull(buf), tphase, abort_flag, args.dev_status, args.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_addr + buf * BN;
+          if (!warp_live) {
+            // nothing to read
+          } else if (FP8) {
+            // promotion of this K block: acc += partial * (s_a[row, kb] * s_w[block, kb])
+            const float sa = row_ok ? args.a_scales[(size_t)row * kbs_total + rd] : 0.0f;
+            const float s0 = cols_ok ? wsc[ws0 + rd] * sa : 0.0f;
+            const float s1 = cols_ok ? wsc[ws1 + rd] * sa : 0.0f;
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+                                      : 128 * half + 32 * c;
+              uint32_t r[32];
+              tmem_ld32(tb + tcol, r);
+              tmem_wait_ld();
+              const float sc = (SWIGLU && c >= 2) ? s1 : s0;
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * c + i]);
+            }
+          } else {
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+                                      : 128 * half + 32 * c;
+              uint32_t r[32];
+              tmem_ld32(tb + tcol, r);
+              tmem_wait_ld();
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) acc[32 * c + i] = __uint_as_float(r[i]);
             }
           }
-          unsigned m = __ballot_sync(0xffffffffu, done_t >= 0);
-          if (m) __threadfence();
-          while (m) {
-            const int l = __ffs(m) - 1;
-            m &= m - 1;
-            combine_block(args, __shfl_sync(0xffffffffu, done_t, l), col0, lane);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(buf));
+          if (++buf == 2) {
+            buf = 0;
+            tphase ^= 1;
+          }
+        }
+        // FP8 SwiGLU: the eight warps exchange row maxima through a named barrier below, so
+        // they agree on leaving (one reduction per unit on every warp) before any of them does
+        if (FP8 && SWIGLU) {
+          if (bar_red_or(1, 32 * EPI_WARPS, !ok)) break;
+        } else if (!ok) {
+          break;
+        }
+        // ---- tile epilogue from registers
+        if (SWIGLU) {
+          float h[64];
+  #pragma unroll
+          for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
+          if (!FP8) {
+            if (row_ok && cols_ok) store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+          } else {
+            // 1x128 block of h = this thread's 64 columns + the partner half's 64
+            float amax = 0.0f;
+  #pragma unroll
+            for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(h[i]));
+            xch[half * 128 + r_in_tile] = amax;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            amax = fmaxf(amax, xch[(1 - half) * 128 + r_in_tile]);
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            const float s = block_scale(amax);
+            if (row_ok && cols_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + (size_t)row * out_cols + col0);
+  #pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t o[4];
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t word = 0;
+  #pragma unroll
+                  for (int b = 0; b < 4; ++b) word |= (uint32_t)f32_to_e4m3(__fdiv_rn(h[16 * v + 4 * j + b], s)) << (8 * b);
+                  o[j] = word;
+                }
+                dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+              }
+              if (half == 0) args.out_scales[(size_t)row * (out_cols / 128) + w.nt] = s;
+            }
+          }
+        } else if (cols_ok) {
+          if (args.row_scale) {
+            // router weight of each permuted row, applied to the float32 accumulator
+            const float rs = row_ok ? args.row_scale[row] : 0.0f;
+  #pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
+          }
+          const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
+          store_rows_bf16(acc, stage_out + (warp - 2) * STAGE_OUT_BYTES, lane, rows_here,
+                          static_cast<uint16_t*>(args.out), w.row0 + 32 * q, out_cols, col0);
+          if (FUSE) {
+            // Rows [row0 + 32q, + rows_here) x columns [col0, col0 + 128) are stored.  Each lane
+            // counts its row in the (token, 128-column block) counter; the lane whose count
+            // completes the token's rows (its valid slots + its shared row) has its warp sum
+            // the block.  Every lane's stores are fenced before the counts (release); the
+            // summing warp fences again before it reads the rows (acquire).  No CTA waits.
+            __threadfence();
+            __syncwarp();
+            int done_t = -1;
+            if (lane < rows_here) {
+              const int src = args.src_row[w.row0 + 32 * q + lane];
+              const int TK = args.T * args.K;
+              const int t = src < TK ? src / args.K : src - TK;
+              if (src >= 0 && t < args.T) {
+                // rows of token t: its valid slots and its shared row (loads issued together)
+                int target = 0;
+                for (int k0 = 0; k0 < args.K; k0 += 8) {
+                  int pv[8];
+  #pragma unroll
+                  for (int j = 0; j < 8; ++j) pv[j] = k0 + j < args.K ? args.inv_map[(size_t)t * args.K + k0 + j] : -1;
+  #pragma unroll
+                  for (int j = 0; j < 8; ++j) target += pv[j] >= 0;
+                }
+                if (args.shared_map && args.shared_map[t] >= 0) ++target;
+                int32_t* cnt = args.counters + (size_t)t * (args.n_dim / 128) + col0 / 128;
+                if (atomicAdd(cnt, 1) == target - 1) {
+                  *cnt = 0;   // every row of this block has arrived: reset for the next call
+                  done_t = t;
+                }
+              }
+            }
+            unsigned m = __ballot_sync(0xffffffffu, done_t >= 0);
+            if (m) __threadfence();
+            while (m) {
+              const int l = __ffs(m) - 1;
+              m &= m - 1;
+              combine_block(args, __shfl_sync(0xffffffffu, done_t, l), col0, lane);
+            }
           }
         }
       }

@@ -18,9 +18,9 @@
 // the grid, BF16 and not fused, when the launch has at least 16 units per CTA) take the
 // segments of at most NS rows: such a segment is a weight stream, so its CTAs keep six
 // 32 KB weight tiles in flight behind 4 KB token tiles and issue MMAs with the weights as
-// the M = 128 operand and the segment's rows as N = NS, on one pipeline lane (gate/up) or
-// two (down: two TMA threads, two MMA threads, alternate K blocks).  Every CTA derives the
-// same ny from the segment lengths and a per-unit cost model, so no host sync is needed.
+// the M = 128 operand and the segment's rows as N = NS, on two pipeline lanes (two TMA
+// threads, two MMA threads, alternate K blocks).  Every CTA derives the same ny from the
+// segment lengths and a per-unit cost model, so no host sync is needed.
 //
 // Warp roles of the MMA pipeline (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane)
@@ -29,15 +29,15 @@
 //               half (w-2)/4 of the tile's columns.
 // TMEM: 512 columns = two 256-column accumulator buffers, so the epilogue of one
 // accumulation round overlaps the MMAs of the next.
-//   BF16: one round per tile; the whole K loop accumulates in TMEM.
+//   BF16: one round per tile; the whole K loop accumulates in TMEM.  BF16 gate/up (not
+//         fused) computes two M-tiles per unit instead, one accumulator each (below).
 //   E4M3: one round per 128-wide K block: each block's partial product is scaled by its
 //         activation scale (per row) and weight scale (per 128x128 block) and added into
 //         float32 registers by the epilogue warps ("promotion"), since the scales are
 //         float32 per 128 elements rather than a format the MMA applies itself.
 //
 // Warp roles of a streaming CTA: warps 0 and 6 TMA producers of pipeline lanes 0 and 1,
-// warps 1 and 7 their MMA issuers (warp 1 also allocates TMEM), warps 2..5 epilogue; with
-// one lane, warps 6 and 7 idle.
+// warps 1 and 7 their MMA issuers (warp 1 also allocates TMEM), warps 2..5 epilogue.
 //
 // Every mbarrier wait is bounded (about 2 s of globaltimer); on expiry the CTA sets
 // MOE_DEV_PIPELINE_TIMEOUT in the status word, every role leaves its loop, the producers
@@ -95,23 +95,22 @@ struct SmemLayout {
 };
 static_assert(SmemLayout::costs + 8 <= SmemLayout::arrays, "common tail header");
 static_assert(STAGES <= YSTAGES, "barrier slots");
-// Streaming pipeline lanes per GEMM: the down projection streams on two lanes, gate/up on
-// one.  Two lanes make a streamed unit 1.5 times faster, but the faster weight stream takes
-// L2 and HBM bandwidth from the MMA pipeline, whose gate/up units (3.7 MB of weights per
-// N-tile) lose more than the streaming role gains: in same-box A/B runs gate/up was 1.4 %
-// faster on one lane, down 1.5 % faster on two.
+// Streaming pipeline lanes: two for both GEMMs.  (With one M-tile per gate/up unit one lane
+// was faster for gate/up: the faster weight stream took L2 and HBM bandwidth from that
+// pipeline.  With two M-tiles per unit, which needs a third fewer operand bytes per product,
+// two lanes are faster: gate/up 3.26-3.38 against 3.40-3.42 ms in same-box A/B runs.)
 template <bool SWIGLU>
-__host__ __device__ constexpr int y_lanes() { return SWIGLU ? 1 : 2; }
+__host__ __device__ constexpr int y_lanes() { return 2; }
 // Relative time of one unit (all units of a launch have the same K): an MMA-bound tile, a
-// single-tile segment's tile on the MMA pipeline, and a streamed unit.  They set how many
-// CTAs stream.  Measured per unit on the prefill expert mix with both roles running: an
-// MMA-pipeline unit about 45 us on gate/up and 13 us on down, a streamed unit 50.7 us on one
-// lane (gate/up) and 11 us on two (down); each streamed cost is set above its measurement
-// so that the streaming CTAs, which cannot hand work back, do not finish last (with two
-// lanes, 24 streaming CTAs of 152 timed best).
-constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM_1LANE = 53.5f, COST_STREAM_2LANES = 42.0f;
-// two-tile unit of the gate/up pipeline (relative to COST_MMA per single tile)
-constexpr float COST_MMA2 = 84.0f;
+// single-tile segment's tile on the MMA pipeline, a two-tile gate/up unit, and a streamed
+// unit.  They set how many CTAs stream.  Measured per unit on the prefill expert mix with
+// both roles running: a one-tile unit about 45 us on gate/up and 13 us on down, a streamed
+// unit 37 and 11 us; the streamed cost is set above its measurement so that the streaming
+// CTAs, which cannot hand work back, do not finish last.  The two-tile cost was swept:
+// 92 gave 24 streaming CTAs and 40 rounds of gate/up units on the other 128 (gate/up
+// 3.26-3.38 ms), 84-88 gave 25-26 streaming CTAs and 41 rounds (3.51-3.59 ms).
+constexpr float COST_MMA = 46.0f, COST_SINGLE = 61.0f, COST_STREAM = 42.0f;
+constexpr float COST_MMA2 = 92.0f;
 // Streaming CTAs: warps 0 and Y_PRODUCER1 load the ring, warps 1 and Y_ISSUER1 issue the
 // MMAs (one pair per pipeline lane), warps 2..5 are the epilogue (one unit streams for tens
 // of microseconds; its epilogue is short).
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int l = len(s);
       if (streamed(l)) {
         ++local_y;
-        cy += y_lanes<SWIGLU>() == 2 ? COST_STREAM_2LANES : COST_STREAM_1LANE;
+        cy += COST_STREAM;
       } else {
         const int m = (l + BM - 1) / BM;
         local += M2 ? (m + 1) / 2 : m;
@@ -313,6 +312,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     return w;
   };
   // CTAs [gx, gridDim.x) stream; every CTA derives the same split from the same counts.
+  // The estimate ny = the streaming share of the modelled time, then the split near it whose
+  // slower role, counted in whole rounds of units (ceil(units / CTAs) x the role's mean unit
+  // cost), ends first: a gate/up unit of two M-tiles runs for tens of microseconds, so one
+  // more round of units on the MMA pipeline costs more than the proportional model sees.
   int ny = 0;
   if (total_y > 0) {
     const int G = gridDim.x;
@@ -320,8 +323,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       ny = G;
     } else {
       const float f = costs[1] / (costs[0] + costs[1]);
-      ny = static_cast<int>(f * static_cast<float>(G) + 0.5f);
-      ny = min(max(ny, 1), G - 1);
+      const int est = min(max(static_cast<int>(f * static_cast<float>(G) + 0.5f), 1), G - 1);
+      const float cx_unit = costs[0] / static_cast<float>(prefix[nseg]);
+      const float cy_unit = costs[1] / static_cast<float>(prefix_y[nseg]);
+      float best = 0.0f;
+      for (int c = max(1, est - 8); c <= min(G - 1, est + 8); ++c) {
+        const float tx = static_cast<float>((total_units + G - c - 1) / (G - c)) * cx_unit;
+        const float ty = static_cast<float>((total_y + c - 1) / c) * cy_unit;
+        const float t = fmaxf(tx, ty);
+        if (ny == 0 || t < best) {
+          best = t;
+          ny = c;
+        }
+      }
     }
   }
   const int gx = static_cast<int>(gridDim.x) - ny;
@@ -382,9 +396,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // two 128-row halves of the weight tile are the A operands of two MMAs (M = 128) that
       // share the segment's NS token rows as B (N = NS).
       // The K blocks of this CTA's units, numbered g = 0, 1, ... in order, run on kLanes
-      // lanes of the pipeline (y_lanes: two for the down projection, one for gate/up): lane p
-      // (producer thread p, MMA thread p) takes the K blocks with g % kLanes == p, which with
-      // two lanes live in the stages of parity p (stage g % YSTAGES, YSTAGES even), and
+      // lanes of the pipeline (y_lanes, two): lane p (producer thread p, MMA thread p) takes
+      // the K blocks with g % kLanes == p, which with two lanes live in the stages of parity
+      // p (stage g % YSTAGES, YSTAGES even), and
       // accumulates into its own TMEM columns; the epilogue adds lane 0's sum (even K
       // blocks) and lane 1's (odd K blocks), in that order.  k_dim is a multiple of 128, so
       // a unit has an even number of 64-wide K blocks and g % 2 == kb % 2.  A single MMA

@@ -26,9 +26,9 @@
 //     g and u side by side for its rows; plain: weight rows [256 nt + 128 r, +128) on rank r).
 //   Streaming pairs (segments of at most NS rows, when the launch has many units): the
 //     weights are the M operand (128 rows per CTA) and the segment's rows the N operand
-//     (N = NS, NS / 2 rows per CTA), through a 10-stage ring of 18 KB stages per CTA, run
-//     for the down projection as two lanes (alternate K blocks, two TMA threads per CTA,
-//     two MMA threads in the leader, even and odd K blocks summed apart and then added).  For
+//     (N = NS, NS / 2 rows per CTA), through a 10-stage ring of 18 KB stages per CTA run as
+//     two lanes (alternate K blocks, two TMA threads per CTA, two MMA threads in the
+//     leader, even and odd K blocks summed apart and then added).  For
 //     SwiGLU rank r holds gate rows [128 nt + 64 r, +64) and the matching up rows, so its
 //     tensor memory lanes 0-63 hold g and lanes 64-127 u of the same 64 output columns.
 //
@@ -60,11 +60,10 @@ constexpr int QT_ROWS = NS / 2;                      // token rows per CTA
 constexpr int QT_BYTES = QT_ROWS * KB_BYTES;         // 2 KB
 constexpr int Q_STAGE_BYTES = B_HALF + QT_BYTES;     // 18 KB, a multiple of 1024
 constexpr int Q_EPI_WARPS = 4;
-// Streaming pairs run as many pipeline lanes as the single-CTA kernel's streaming CTAs (one
-// for gate/up, two for the down projection), with the same order of sums.  With two lanes,
-// lane p (a TMA thread in each CTA, an MMA thread in the leader) takes the K blocks with
-// g % 2 == p of the pair's sequence, in the stages of parity p.  Lane 0 uses warps 0 and 1,
-// lane 1 the two warps after the streaming epilogue's.
+// Streaming pairs run two pipeline lanes, like the single-CTA kernel's streaming CTAs, with
+// the same order of sums: lane p (a TMA thread in each CTA, an MMA thread in the leader)
+// takes the K blocks with g % 2 == p of the pair's sequence, in the stages of parity p.
+// Lane 0 uses warps 0 and 1, lane 1 the two warps after the streaming epilogue's.
 constexpr int Q_PRODUCER1 = 2 + Q_EPI_WARPS, Q_ISSUER1 = Q_PRODUCER1 + 1;
 static_assert(Q_ISSUER1 < THREADS / 32, "streaming warps");
 constexpr int Q_XPITCH = 17;                         // floats per lane row of the exchange (conflict-free)
@@ -107,10 +106,9 @@ static_assert(Q_STAGE_BYTES % 1024 == 0 && P_STAGE_TX % 1024 == 0, "swizzle atom
 // M-tiles of a segment with more than one M-tile, the single M-tile of a short segment on
 // the MMA pipeline (its 256 weight rows stream from HBM behind a shallow ring), and a
 // streamed segment.  They set how many pairs stream.  Measured per unit on the prefill
-// expert mix with both roles running (gate/up: about 41 us per pipeline unit, 47 us per
-// streamed unit on one streaming lane; a streamed down-projection unit on two lanes costs
-// about three quarters of a pipeline unit).
-constexpr float COSTP_MMA = 40.0f, COSTP_SINGLE = 45.0f, COSTP_STREAM_1LANE = 47.0f, COSTP_STREAM_2LANES = 31.0f;
+// expert mix with both roles running (gate/up: about 41 us per pipeline unit, 31 us per
+// streamed unit on the two streaming lanes).
+constexpr float COSTP_MMA = 40.0f, COSTP_SINGLE = 45.0f, COSTP_STREAM = 31.0f;
 
 // ------------------------------------------------------------------ cluster / pair PTX
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -297,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int l = len(s);
       if (streamed(l)) {
         ++local_y;
-        cy += SWIGLU ? COSTP_STREAM_1LANE : COSTP_STREAM_2LANES;
+        cy += COSTP_STREAM;
       } else {
         const int m = (l + BM - 1) / BM;
         const int mp = (m + 1) / 2;
@@ -367,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_tfull(b), y_role && !SWIGLU ? 2 : 1);                 // streaming: one per lane
+      mbar_init(bar_tfull(b), y_role ? 2 : 1);                            // streaming: one per lane
       mbar_init(bar_tempty(b), 2 * (y_role ? Q_EPI_WARPS : EPI_WARPS));   // both CTAs' epilogue warps
     }
     mbar_init(bar_drain, 1);
@@ -418,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int u_step = y_role ? nyp : gxu;
   const int mgroup = SWIGLU ? MGROUP_GATE_UP / 2 : 0;
 
-  if (warp == 0 || (y_role && !SWIGLU && warp == Q_PRODUCER1)) {
+  if (warp == 0 || (y_role && warp == Q_PRODUCER1)) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     // (streaming: lane p = 0, 1 fills the stages of parity p)
     if (lane == 0) {
@@ -464,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         for (int kb = 0; kb < kblocks; ++kb, ++g) {
-          if (y_role && !SWIGLU && (g & 1u) != lp) {   // the other lane's K block
+          if (y_role && (g & 1u) != lp) {   // the other lane's K block
             if (++stage == nst) {
               stage = 0;
               phase ^= 1;
@@ -536,7 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (armed & (1u << s)) pdrain(bar_empty(s), (last_parity >> s) & 1u);
       }
     }
-  } else if (warp == 1 || (y_role && !SWIGLU && warp == Q_ISSUER1)) {
+  } else if (warp == 1 || (y_role && warp == Q_ISSUER1)) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer (leader; streaming:
       // lane p = 0, 1 consumes the stages of parity p)
@@ -556,7 +554,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
           }
-          if (y_role && !SWIGLU && (g & 1u) != lp) {   // the other lane's K block
+          if (y_role && (g & 1u) != lp) {   // the other lane's K block
             if (++stage == nst) {
               stage = 0;
               phase ^= 1;
@@ -576,11 +574,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             sa = sbase + PairSmem::a + stage * A_BYTES;
             sb = sbase + PairSmem::b + stage * B_HALF;
           }
-          // streaming pairs on two lanes (down): even and odd K blocks accumulate apart (columns
-          // [2 NS b, +NS) and [2 NS b + NS, +NS)) and the epilogue adds the two sums, the order
-          // of the single-CTA kernel's two streaming lanes (k_dim % 128 == 0: an even K-block
-          // count); on one lane (gate/up) one sum, as there
-          const bool split = y_role && !SWIGLU;
+          // streaming pairs: even and odd K blocks accumulate apart (columns [2 NS b, +NS) and
+          // [2 NS b + NS, +NS)) and the epilogue adds the two sums, the order of the single-CTA
+          // kernel's two streaming lanes (k_dim % 128 == 0: an even K-block count)
+          const bool split = y_role;
           const uint32_t dt = y_role ? tmem_base + buf * (2 * NS) + ((split && (kb & 1)) ? NS : 0) : tmem_base + buf * acc_cols;
           const int kfirst = split ? (kb >> 1) : kb;
 #pragma unroll
@@ -688,7 +685,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t d[NS];
       tmem_ld32(tmem_base + lane_addr + buf * (2 * NS), d);
       tmem_wait_ld();
-      if (!SWIGLU) {
+      {
         uint32_t e[NS];
         tmem_ld32(tmem_base + lane_addr + buf * (2 * NS) + NS, e);
         tmem_wait_ld();

@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool cols_ok = col0 < out_cols;
         float acc[128];
         if (FP8) {
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
         }
         const bool extra = w.seg >= args.num_w;
@@ -843,7 +843,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float sa = row_ok ? args.a_scales[(size_t)row * kbs_total + rd] : 0.0f;
             const float s0 = cols_ok ? wsc[ws0 + rd] * sa : 0.0f;
             const float s1 = cols_ok ? wsc[ws1 + rd] * sa : 0.0f;
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
                                       : 128 * half + 32 * c;
@@ -851,18 +851,18 @@ __global__ void __launch_bounds__(THREADS, 1)
               tmem_ld32(tb + tcol, r);
               tmem_wait_ld();
               const float sc = (SWIGLU && c >= 2) ? s1 : s0;
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * c + i]);
             }
           } else {
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
                                       : 128 * half + 32 * c;
               uint32_t r[32];
               tmem_ld32(tb + tcol, r);
               tmem_wait_ld();
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i) acc[32 * c + i] = __uint_as_float(r[i]);
             }
           }
@@ -884,14 +884,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---- tile epilogue from registers
         if (SWIGLU) {
           float h[64];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
           if (!FP8) {
             if (row_ok && cols_ok) store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
           } else {
             // 1x128 block of h = this thread's 64 columns + the partner half's 64
             float amax = 0.0f;
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(h[i]));
             xch[half * 128 + r_in_tile] = amax;
             asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -900,13 +900,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float s = block_scale(amax);
             if (row_ok && cols_ok) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + (size_t)row * out_cols + col0);
-  #pragma unroll
+#pragma unroll
               for (int v = 0; v < 4; ++v) {
                 uint32_t o[4];
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   uint32_t word = 0;
-  #pragma unroll
+#pragma unroll
                   for (int b = 0; b < 4; ++b) word |= (uint32_t)f32_to_e4m3(__fdiv_rn(h[16 * v + 4 * j + b], s)) << (8 * b);
                   o[j] = word;
                 }
@@ -919,7 +919,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (args.row_scale) {
             // router weight of each permuted row, applied to the float32 accumulator
             const float rs = row_ok ? args.row_scale[row] : 0.0f;
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
           }
           const int rows_here = w.row_end - (w.row0 + 32 * q);   // rows of this warp's 32 in the segment
@@ -943,9 +943,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int target = 0;
                 for (int k0 = 0; k0 < args.K; k0 += 8) {
                   int pv[8];
-  #pragma unroll
+#pragma unroll
                   for (int j = 0; j < 8; ++j) pv[j] = k0 + j < args.K ? args.inv_map[(size_t)t * args.K + k0 + j] : -1;
-  #pragma unroll
+#pragma unroll
                   for (int j = 0; j < 8; ++j) target += pv[j] >= 0;
                 }
                 if (args.shared_map && args.shared_map[t] >= 0) ++target;

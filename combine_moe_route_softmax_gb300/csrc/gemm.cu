@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr bool M2 = SWIGLU && !FP8 && !FUSE;   // two M-tiles per MMA-pipeline unit
+  constexpr bool M2 = !FP8 && !FUSE;   // two M-tiles per MMA-pipeline unit
   uint8_t* cmn = smem + args.common_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(cmn);
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // pairs of M-tiles, so the decoder's row0 is the segment start + (pair index) * BM)
   auto mma_unit = [&](int u) {
     Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok,
-                         M2 ? MGROUP_GATE_UP / 2 : (SWIGLU && !FP8 ? MGROUP_GATE_UP : 0));
+                         SWIGLU && !FP8 ? (M2 ? MGROUP_GATE_UP / 2 : MGROUP_GATE_UP) : 0);
     if (M2) {
       const int b0 = seg_begin(cu_s, w.seg, mtok);
       w.row0 = b0 + 2 * (w.row0 - b0);
@@ -758,12 +758,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       zero_rowless_tokens(args, blockIdx.x * EPI_WARPS + (warp - 2), active * EPI_WARPS, lane);
     }
     if constexpr (M2) {
-      // two-tile units (BF16 gate/up): read accumulator 0, free it, compute and store M-tile
-      // 0's h; then accumulator 1 (freed at once when the unit has one M-tile) and M-tile 1
+      // two-tile units (BF16, not fused): read accumulator 0, free it, compute and store
+      // M-tile 0's rows; then accumulator 1 (freed at once when the unit has one M-tile) and
+      // M-tile 1
       for (int u = blockIdx.x; u < total_units; u += gxu) {
         const Unit w = mma_unit(u);
         const bool two = w.row0 + BM < w.row_end;
-        const int col0 = w.nt * 128 + 64 * half;
+        const int col0 = SWIGLU ? w.nt * 128 + 64 * half : w.nt * BN + 128 * half;
         const bool cols_ok = col0 < out_cols;
         if (!mbar_wait(bar_tfull(0), tphase, abort_flag, args.dev_status, args.timeout_ns)) break;
         tc_fence_after();
@@ -777,7 +778,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t tb = tmem_base + lane_addr + t * BN;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int tcol = c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2);
+            const int tcol = SWIGLU ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+                                    : 128 * half + 32 * c;
             uint32_t r[32];
             tmem_ld32(tb + tcol, r);
             tmem_wait_ld();
@@ -787,12 +789,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(t));
-          const int row = w.row0 + t * BM + r_in_tile;
-          if (row < w.row_end && cols_ok) {
-            float h[64];
+          const int trow0 = w.row0 + t * BM;   // first row of M-tile t
+          const int row = trow0 + r_in_tile;
+          if (SWIGLU) {
+            if (row < w.row_end && cols_ok) {
+              float h[64];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
-            store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+              for (int i = 0; i < 64; ++i) h[i] = silu(acc[i]) * acc[64 + i];
+              store_h_bf16(h, static_cast<uint16_t*>(args.out) + (size_t)row * out_cols + col0);
+            }
+          } else if (cols_ok) {
+            if (args.row_scale) {
+              // router weight of each permuted row, applied to the float32 accumulator
+              const float rs = row < w.row_end ? args.row_scale[row] : 0.0f;
+#pragma unroll
+              for (int i = 0; i < 128; ++i) acc[i] = __fmul_rn(acc[i], rs);
+            }
+            const int rows_here = w.row_end - (trow0 + 32 * q);   // rows of this warp's 32 in the segment
+            store_rows_bf16(acc, stage_out + (warp - 2) * STAGE_OUT_BYTES, lane, rows_here,
+                            static_cast<uint16_t*>(args.out), trow0 + 32 * q, out_cols, col0);
           }
         }
         tphase ^= 1;

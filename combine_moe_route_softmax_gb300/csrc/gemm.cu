@@ -9,7 +9,8 @@
 // up are one fused weight with 2n rows; FP8 weights carry block_n x block_k scales.
 //
 // Tile: BM = 128 rows x BN = 256 weight rows x 128 bytes of K per pipeline stage
-// (64 BF16 or 128 E4M3 elements), 4 stages (48 KB each).  For SwiGLU the 256 weight rows
+// (64 BF16 or 128 E4M3 elements), 4 stages (48 KB each); BF16 (not fused) units take two
+// such M-tiles sharing the weight tile, 3 stages of 64 KB.  For SwiGLU the 256 weight rows
 // of a tile are 128 gate rows and the matching 128 up rows, so one MMA with N = 256
 // yields g and u for 128 output columns side by side in TMEM.
 //

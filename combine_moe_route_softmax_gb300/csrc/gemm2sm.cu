@@ -1,12 +1,11 @@
 // BF16 grouped GEMM on CTA pairs with the 2-SM MMA (tcgen05.mma.cta_group::2), behind
 // moe_grouped_gemm_pairs.  It computes the same products in the same order as the
 // single-CTA kernel (gemm.cu), and its output is identical bit for bit.  Measured on GB300:
-// per SM its MMA pipeline runs a K step in 0.36 us against 0.40 us, but a streamed unit
-// costs its two SMs 1.7 times the SM time of a single streaming CTA, and a pair always
-// computes two M-tiles of one expert, so on the prefill expert mix it is slower (layer 6.29
-// against 5.99 ms per step on one box: gate/up 3.86 against 3.72 ms, down 2.00 against 1.82
-// ms); on dense experts it ties or wins (down projection of 64 experts x 200 rows: 0.351
-// against 0.407 ms).  The layer uses the single-CTA kernel.
+// per SM its MMA pipeline ran a K step in 0.36 us against 0.40 us for one-tile units of one
+// CTA, but a streamed unit costs its two SMs 1.7 times the SM time of a single streaming
+// CTA; since the single-CTA kernel moved to units of two M-tiles it is faster still (layer
+// 5.34 against 6.04 ms per step on the prefill expert mix, one box).  The layer uses the
+// single-CTA kernel.
 //
 // MoonEP page: the experts run as grouped matmuls (gate, up, down) over the cu_seqlens
 // segments.  This kernel computes them for BF16 operands on pairs of CTAs (clusters of two

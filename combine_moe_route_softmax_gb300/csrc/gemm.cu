@@ -60,6 +60,13 @@ constexpr int STAGE_TX = A_BYTES + B_BYTES;
 // as soon as it has read it, and the next unit's MMAs into it start then (a single buffer
 // cost 0.2-0.6 % on the one-tile path).
 constexpr int STAGES_M2 = 3;
+// Unit order of two-tile gate/up units: groups of 4 units (8 M-tiles), each pair of N-tiles
+// visiting the group's units before the next pair, so a round of the grid covers every
+// N-tile of a few M-tiles (their A rows read from L2 once per round) and the weights of a
+// segment's N-tiles are shared by the round's groups.  Swept on the prefill routing (same
+// box, three rounds): groups of 4 units 3.29-3.33 ms, 8: 3.30-3.35, 16 (the one-tile
+// order's 32 M-tiles): 3.39-3.44, 32-64: 3.46-3.52.
+constexpr int MGROUP_GATE_UP_M2 = 4;
 constexpr int STAGE_M2_BYTES = 2 * A_BYTES + B_BYTES;   // 64 KB
 static_assert(STAGES_M2 * STAGE_M2_BYTES == STAGES * (A_BYTES + B_BYTES), "same shared memory as the one-tile ring");
 
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // pairs of M-tiles, so the decoder's row0 is the segment start + (pair index) * BM)
   auto mma_unit = [&](int u) {
     Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok,
-                         SWIGLU && !FP8 ? (M2 ? MGROUP_GATE_UP / 2 : MGROUP_GATE_UP) : 0);
+                         SWIGLU && !FP8 ? (M2 ? MGROUP_GATE_UP_M2 : MGROUP_GATE_UP) : 0);
     if (M2) {
       const int b0 = seg_begin(cu_s, w.seg, mtok);
       w.row0 = b0 + 2 * (w.row0 - b0);

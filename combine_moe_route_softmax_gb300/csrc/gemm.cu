@@ -67,6 +67,10 @@ constexpr int STAGES_M2 = 3;
 // box, three rounds): groups of 4 units 3.29-3.33 ms, 8: 3.30-3.35, 16 (the one-tile
 // order's 32 M-tiles): 3.39-3.44, 32-64: 3.46-3.52.
 constexpr int MGROUP_GATE_UP_M2 = 4;
+// The down projection's two-tile units in groups of 8 the same way (its one-tile units kept
+// the M-tile-major order, every N-tile of one M-tile before the next): 1.69-1.73 against
+// 1.74-1.75 ms in same-box sweeps (groups of 2: 1.71-1.75, 16: 1.71-1.73).
+constexpr int MGROUP_DOWN_M2 = 8;
 constexpr int STAGE_M2_BYTES = 2 * A_BYTES + B_BYTES;   // 64 KB
 static_assert(STAGES_M2 * STAGE_M2_BYTES == STAGES * (A_BYTES + B_BYTES), "same shared memory as the one-tile ring");
 
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // pairs of M-tiles, so the decoder's row0 is the segment start + (pair index) * BM)
   auto mma_unit = [&](int u) {
     Unit w = decode_unit(u, n_tiles, cu_s, prefix, nseg, mtok,
-                         SWIGLU && !FP8 ? (M2 ? MGROUP_GATE_UP_M2 : MGROUP_GATE_UP) : 0);
+                         SWIGLU && !FP8 ? (M2 ? MGROUP_GATE_UP_M2 : MGROUP_GATE_UP) : (M2 ? MGROUP_DOWN_M2 : 0));
     if (M2) {
       const int b0 = seg_begin(cu_s, w.seg, mtok);
       w.row0 = b0 + 2 * (w.row0 - b0);

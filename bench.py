@@ -173,7 +173,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------- our arm
 def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_fq=None, weight_in_down=False,
-                   gemm_pairs=False):
+                   gemm_pairs=False, weight_tiles=False):
     import combine_moe_route_softmax_gb300 as moe
     logits = synth.router_logits(w, seed, device=device)
     x = synth.hidden(w, seed, device=device)
@@ -194,7 +194,7 @@ def workload_state(w, seed, device, max_tokens=0, fuse_combine=False, dispatch_f
         dtype = moe.MOE_E4M3
     layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, dtype, max_tokens=max_tokens, fuse_combine=fuse_combine,
                          weight_in_down=weight_in_down, combine_fq=w.fq_format, dispatch_fq=dispatch_fq or "e4m3",
-                         gemm_pairs=gemm_pairs, **kw)
+                         gemm_pairs=gemm_pairs, weight_tiles=weight_tiles, **kw)
     fq = None
     if w.fake_quant:
         # combine fake-quant: the constant scale 448 / amax (E4M3) or the per-tensor scale
@@ -262,6 +262,7 @@ def staged_step(st, w, events):
     s = torch.cuda.current_stream().cuda_stream
     nseg = d.E + d.has_shared
     tw = lay.tensors
+    gdt = d.dtype | (moe.MOE_W_TILED if d.weight_tiles else 0)   # the grouped GEMMs' dtype argument
     p = lambda t: None if t is None else t.data_ptr()
     events[0].record()
     assert L.moe_route_topk(p(st["logits"]), d.T, d.E, d.K, p(st["n"]), p(st["idx"]), p(st["wt"]), s) == 0
@@ -296,20 +297,20 @@ def staged_step(st, w, events):
     events[2].record()
     if mt:
         assert L.moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, nseg, mt, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
-                                          d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                          d.E, p(tw[2]), p(tw[6]), gdt, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                           p(st["status"]), None, s) == 0
     elif d.gemm_pairs:
         assert L.moe_grouped_gemm_pairs(v.xp, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), d.E, p(tw[2]),
                                         moe.MOE_EPI_SWIGLU, v.hs, p(st["status"]), None, s) == 0
     else:
         assert L.moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, nseg, v.cap, d.H, 2 * d.I, p(tw[0]), p(tw[4]),
-                                  d.E, p(tw[2]), p(tw[6]), d.dtype, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                  d.E, p(tw[2]), p(tw[6]), gdt, moe.MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                   p(st["status"]), s) == 0
     events[3].record()
     if d.fuse_combine:
         # down projection + combine in one launch: the combine stage below is empty
         assert L.moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m if mt else v.cu_seqlens, nseg, mt, v.cap,
-                                          d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), d.dtype, v.y, wd_rows,
+                                          d.I, d.H, p(tw[1]), p(tw[5]), d.E, p(tw[3]), p(tw[7]), gdt, v.y, wd_rows,
                                           v.src_row, v.inv_map, None if wd else p(st["wt"]), d.T, d.K, v.shared_map,
                                           p(st["fq"]),
                                           p(st["out"]), v.counters, p(st["status"]), s) == 0
@@ -318,14 +319,14 @@ def staged_step(st, w, events):
         return
     if mt:
         assert L.moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, nseg, mt, d.I, d.H, p(tw[1]), p(tw[5]),
-                                          d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None,
+                                          d.E, p(tw[3]), p(tw[7]), gdt, moe.MOE_EPI_NONE, v.y, None,
                                           p(st["status"]), wd_rows, s) == 0
     elif d.gemm_pairs:
         assert L.moe_grouped_gemm_pairs(v.hs, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), d.E, p(tw[3]),
                                         moe.MOE_EPI_NONE, v.y, p(st["status"]), wd_rows, s) == 0
     else:
         assert L.moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, nseg, v.cap, d.I, d.H, p(tw[1]), p(tw[5]),
-                                     d.E, p(tw[3]), p(tw[7]), d.dtype, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
+                                     d.E, p(tw[3]), p(tw[7]), gdt, moe.MOE_EPI_NONE, v.y, None, p(st["status"]),
                                      wd_rows, s) == 0
     events[4].record()
     if st["fq"] is not None and d.combine_fq_format == 1:
@@ -367,6 +368,12 @@ def algorithmic_work(w, st):
     }
 
 
+def weight_tiles(args):
+    """Whether the layer reads its weights in the tile layout (the SM-pair GEMM reads
+    row-major weights only)."""
+    return args.weights == "tiles" and not args.gemm_pairs
+
+
 def run_ours(args, rank, world, local_rank):
     import combine_moe_route_softmax_gb300 as moe
     device = torch.device("cuda", local_rank)
@@ -375,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
     w = synth.WORKLOADS[args.workload]
     max_tokens = (args.max_tokens or w.T) if args.layout == "batched" else 0
     st = workload_state(w, rank_seed(0, rank), device, max_tokens, args.fuse_combine, args.dispatch_fq,
-                        args.weight_in_down, args.gemm_pairs)
+                        args.weight_in_down, args.gemm_pairs, weight_tiles(args))
     for _ in range(args.warmup):
         layer_step(st)
     torch.cuda.synchronize()
@@ -566,6 +573,8 @@ def run_ours(args, rank, world, local_rank):
                                f"constant scale {float(st['fq'].item()):.5g}" if w.fake_quant else ""),
                    "gemm": ("grouped GEMMs on SM pairs (2-SM MMA)" if args.gemm_pairs
                             else "grouped GEMMs one CTA per tile"),
+                   "weights": ("tile layout (moe_pack_weights, once at setup, untimed)" if weight_tiles(args)
+                               else "row-major [E, N, K]"),
                    "router_weight": ("applied in the down projection's epilogue (weighted rows; the combine sums)"
                                      if args.weight_in_down else "applied in the combine"),
                    "dispatch": (f"{'NVFP4' if args.dispatch_fq == 'nvfp4' else 'E4M3'} fake-quant of the "
@@ -700,6 +709,9 @@ def main():
                     help="BF16: both grouped GEMMs on SM pairs with the 2-SM MMA (moe_grouped_gemm_pairs)")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="run the combine inside the down projection (moe_grouped_gemm_combine)")
+    ap.add_argument("--weights", choices=["tiles", "rows"], default="tiles",
+                    help="expert weights in the tile layout of moe_pack_weights (default; not with --gemm-pairs, "
+                         "which reads row-major weights) or row-major")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="rows per expert block of the batched layout (default: the bucket's T, which never "
                          "overflows)")

@@ -14,6 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 MOE_BF16, MOE_E4M3 = 0, 1
+MOE_W_TILED = 0x100   # ORed into a grouped GEMM dtype: weights in the tile layout of moe_pack_weights
 MOE_EPI_NONE, MOE_EPI_SWIGLU = 0, 1
 MOE_DEV_BAD_EXPERT, MOE_DEV_VERIFY_MISMATCH, MOE_DEV_PIPELINE_TIMEOUT, MOE_DEV_OVERFLOW = 1, 2, 4, 8
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_WORKSPACE", 3: "MOE_ERR_UNSUPPORTED", 4: "MOE_ERR_CUDA"}
@@ -30,7 +31,7 @@ class MoeError(RuntimeError):
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", _I), ("H", _I), ("I", _I), ("E", _I), ("K", _I), ("dtype", _I), ("has_shared", _I),
                 ("weight_in_down", _I), ("max_tokens", _I), ("fuse_combine", _I), ("combine_fq_format", _I),
-                ("dispatch_fq_format", _I), ("gemm_pairs", _I)]
+                ("dispatch_fq_format", _I), ("gemm_pairs", _I), ("weight_tiles", _I)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -63,6 +64,7 @@ _SIGS = {
     "moe_grouped_gemm": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_ex": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_pairs": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P], _I),
+    "moe_pack_weights": ([_P, _I, _I, _I, _I, _P, _P], _I),
     "moe_grouped_gemm_batched": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P],
                                  _I),
     "moe_grouped_gemm_combine": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I,
@@ -237,11 +239,26 @@ def moe_quantize_weight_fp8(w, stream=None):
     return q, s
 
 
+def moe_pack_weights(w, out=None, stream=None):
+    """w [..., n, k] (bf16, or uint8 E4M3 codes) -> a tensor of the same shape and dtype
+    holding the same bytes in the tile layout of moe_pack_weights (pass it with tiled=True
+    or to MoeLayer(weight_tiles=True) only: its rows are not w's rows)."""
+    _dev(w)
+    n, k = w.shape[-2:]
+    mats = w.numel() // (n * k)
+    if out is None:
+        out = torch.empty_like(w)
+    dt = MOE_E4M3 if w.dtype == torch.uint8 else MOE_BF16
+    _check("moe_pack_weights", lib().moe_pack_weights(_ptr(w), mats, n, k, dt, _ptr(out), _stream(stream)))
+    return out
+
+
 def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=None, w_extra=None,
                      w_extra_scales=None, epilogue=MOE_EPI_NONE, out=None, out_scales=None, dev_status=None,
-                     stream=None, row_scale=None, pairs=False):
+                     stream=None, row_scale=None, pairs=False, tiled=False):
     """a [rows_cap, k] (bf16 or uint8 E4M3 codes); w [num_w, n, k]; returns (out, out_scales).
-    pairs=True: the BF16 computation on pairs of SMs (moe_grouped_gemm_pairs)."""
+    pairs=True: the BF16 computation on pairs of SMs (moe_grouped_gemm_pairs); tiled=True: w
+    and w_extra from moe_pack_weights (MOE_W_TILED)."""
     _dev(a)
     fp8 = a.dtype == torch.uint8
     rows_cap, k_dim = a.shape
@@ -254,6 +271,7 @@ def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=
         out = torch.empty(rows_cap, out_cols, dtype=odt, device=a.device)
     if fp8 and epilogue == MOE_EPI_SWIGLU and out_scales is None:
         out_scales = torch.empty(rows_cap, out_cols // 128, dtype=torch.float32, device=a.device)
+    dt = (MOE_E4M3 if fp8 else MOE_BF16) | (MOE_W_TILED if tiled else 0)
     if pairs:
         _check("moe_grouped_gemm_pairs", lib().moe_grouped_gemm_pairs(
             _ptr(a), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), num_w, _ptr(w_extra), epilogue,
@@ -261,19 +279,19 @@ def moe_grouped_gemm(a, cu_seqlens, w, n_segments=None, a_scales=None, w_scales=
     elif row_scale is None:
         _check("moe_grouped_gemm", lib().moe_grouped_gemm(
             _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
-            num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),
+            num_w, _ptr(w_extra), _ptr(w_extra_scales), dt, epilogue, _ptr(out),
             _ptr(out_scales), _ptr(dev_status), _stream(stream)))
     else:
         _check("moe_grouped_gemm_ex", lib().moe_grouped_gemm_ex(
             _ptr(a), _ptr(a_scales), _ptr(cu_seqlens), n_segments, rows_cap, k_dim, n_dim, _ptr(w), _ptr(w_scales),
-            num_w, _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out),
+            num_w, _ptr(w_extra), _ptr(w_extra_scales), dt, epilogue, _ptr(out),
             _ptr(out_scales), _ptr(dev_status), _ptr(row_scale), _stream(stream)))
     return out, out_scales
 
 
 def moe_grouped_gemm_batched(a, masked_m, w, a_scales=None, w_scales=None, w_extra=None, w_extra_scales=None,
                              epilogue=MOE_EPI_NONE, out=None, out_scales=None, dev_status=None, stream=None,
-                             row_scale=None):
+                             row_scale=None, tiled=False):
     """a [S, max_tokens, k] (bf16 or uint8 E4M3 codes), masked_m int32 [S]; w [num_w, n, k];
     returns (out [S, max_tokens, n_out], out_scales)."""
     _dev(a)
@@ -288,14 +306,14 @@ def moe_grouped_gemm_batched(a, masked_m, w, a_scales=None, w_scales=None, w_ext
         out_scales = torch.empty(S, max_tokens, out_cols // 128, dtype=torch.float32, device=a.device)
     _check("moe_grouped_gemm_batched", lib().moe_grouped_gemm_batched(
         _ptr(a), _ptr(a_scales), _ptr(masked_m), S, max_tokens, k_dim, n_dim, _ptr(w), _ptr(w_scales), num_w,
-        _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, epilogue, _ptr(out), _ptr(out_scales),
-        _ptr(dev_status), _ptr(row_scale), _stream(stream)))
+        _ptr(w_extra), _ptr(w_extra_scales), (MOE_E4M3 if fp8 else MOE_BF16) | (MOE_W_TILED if tiled else 0),
+        epilogue, _ptr(out), _ptr(out_scales), _ptr(dev_status), _ptr(row_scale), _stream(stream)))
     return out, out_scales
 
 
 def moe_grouped_gemm_combine(a, seg, w, src_row, inv_map, topk_w, max_tokens=0, shared_map=None, fq_scale=None,
                              a_scales=None, w_scales=None, w_extra=None, w_extra_scales=None, row_scale=None, y=None,
-                             out=None, counters=None, dev_status=None, stream=None):
+                             out=None, counters=None, dev_status=None, stream=None, tiled=False):
     """Down projection with the combine fused: a [rows, k] (or [S, max_tokens, k] with seg =
     masked_m and max_tokens > 0; else seg = cu_seqlens), w [num_w, H, k]; returns (out [T, H],
     y [rows, H], counters)."""
@@ -314,9 +332,9 @@ def moe_grouped_gemm_combine(a, seg, w, src_row, inv_map, topk_w, max_tokens=0, 
         counters = torch.zeros(T, H // 128, dtype=torch.int32, device=a.device)
     _check("moe_grouped_gemm_combine", lib().moe_grouped_gemm_combine(
         _ptr(a), _ptr(a_scales), _ptr(seg), nseg, max_tokens, rows, k_dim, H, _ptr(w), _ptr(w_scales), num_w,
-        _ptr(w_extra), _ptr(w_extra_scales), MOE_E4M3 if fp8 else MOE_BF16, _ptr(y), _ptr(row_scale), _ptr(src_row),
-        _ptr(inv_map), _ptr(topk_w), T, K, _ptr(shared_map), _ptr(fq_scale), _ptr(out), _ptr(counters),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(w_extra), _ptr(w_extra_scales), (MOE_E4M3 if fp8 else MOE_BF16) | (MOE_W_TILED if tiled else 0),
+        _ptr(y), _ptr(row_scale), _ptr(src_row), _ptr(inv_map), _ptr(topk_w), T, K, _ptr(shared_map),
+        _ptr(fq_scale), _ptr(out), _ptr(counters), _ptr(dev_status), _stream(stream)))
     return out, y, counters
 
 
@@ -384,15 +402,20 @@ def moe_fq4_scale_from_amax(amax, scale=None, stream=None):
 class MoeLayer:
     """Holds a layer's descriptor, weight pointers and workspace; forward() is one
     moe_layer_forward call.  Weights: w13 [E, 2I, H], w2 [E, H, I] (+ shared [2I, H],
-    [H, I]) in BF16, or E4M3 codes with their 128x128 scales for dtype MOE_E4M3."""
+    [H, I]) in BF16, or E4M3 codes with their 128x128 scales for dtype MOE_E4M3.
+    weight_tiles=True: the layer keeps copies of the four weight tensors in the tile layout
+    of moe_pack_weights (made once here) and computes from those."""
 
     def __init__(self, T, H, I, E, K, dtype=MOE_BF16, w13=None, w2=None, shared_w13=None, shared_w2=None,
                  w13_scales=None, w2_scales=None, shared_w13_scales=None, shared_w2_scales=None, device="cuda",
                  weight_in_down=False, max_tokens=0, fuse_combine=False, combine_fq="e4m3", dispatch_fq="e4m3",
-                 gemm_pairs=False):
+                 gemm_pairs=False, weight_tiles=False):
         self.desc = LayerDesc(T, H, I, E, K, dtype, int(shared_w13 is not None), int(weight_in_down),
                               int(max_tokens), int(fuse_combine), _fmt(combine_fq), _fmt(dispatch_fq),
-                              int(gemm_pairs))
+                              int(gemm_pairs), int(weight_tiles))
+        if weight_tiles:
+            w13, w2, shared_w13, shared_w2 = (None if t is None else moe_pack_weights(t)
+                                              for t in (w13, w2, shared_w13, shared_w2))
         self.tensors = (w13, w2, shared_w13, shared_w2, w13_scales, w2_scales, shared_w13_scales, shared_w2_scales)
         self.weights = LayerWeights(_ptr(w13), _ptr(w13_scales), _ptr(w2), _ptr(w2_scales), _ptr(shared_w13),
                                     _ptr(shared_w13_scales), _ptr(shared_w2), _ptr(shared_w2_scales))

@@ -400,6 +400,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   constexpr int KE = FP8 ? 128 : 64;  // K elements per stage
   const int kblocks = args.k_dim / KE;
+  // Box of 128 weight rows from r0 (a multiple of 128) and K block kb: at (kb * KE, r0) in
+  // the row-major weights, or in the tile layout ([tiles * 128, KE], tile (r0 / 128, kb) of
+  // a matrix at rows 128 * ((r0 / 128) * kblocks + kb)), where the box is 16 contiguous KB.
+  const bool w_tiled = args.w_tiled != 0;
+  auto wx = [&](int kb) { return w_tiled ? 0 : kb * KE; };
+  auto wy = [&](int r0, int kb) { return w_tiled ? ((r0 >> 7) * kblocks + kb) << 7 : r0; };
 
   if (y_role) {
     if constexpr (!FP8 && !FUSE) {
@@ -462,11 +468,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                 const uint32_t sw = sbase + stage * YSTAGE_BYTES;
                 if (STREAM_EVICT_FIRST) {
-                  tma_load_2d_hint(sw, mb, kb * KE, rA, bar_full(stage), wpol);
-                  tma_load_2d_hint(sw + B_HALF, mb, kb * KE, rB, bar_full(stage), wpol);
+                  tma_load_2d_hint(sw, mb, wx(kb), wy(rA, kb), bar_full(stage), wpol);
+                  tma_load_2d_hint(sw + B_HALF, mb, wx(kb), wy(rB, kb), bar_full(stage), wpol);
                 } else {
-                  tma_load_2d(sw, mb, kb * KE, rA, bar_full(stage));
-                  tma_load_2d(sw + B_HALF, mb, kb * KE, rB, bar_full(stage));
+                  tma_load_2d(sw, mb, wx(kb), wy(rA, kb), bar_full(stage));
+                  tma_load_2d(sw + B_HALF, mb, wx(kb), wy(rB, kb), bar_full(stage));
                 }
                 tma_load_2d(sw + B_BYTES, &tmAt, kb * KE, row0, bar_full(stage));
               }
@@ -630,14 +636,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t sb = sa + 2 * A_BYTES;
             tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
             if (two) tma_load_2d(sa + A_BYTES, &tmA, kb * KE, w.row0 + BM, bar_full(stage));
-            tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
-            tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
+            tma_load_2d(sb, mb, wx(kb), wy(rA, kb), bar_full(stage));
+            tma_load_2d(sb + B_HALF, mb, wx(kb), wy(rB, kb), bar_full(stage));
           } else {
             const uint32_t sa = sbase + SmemLayout::a + stage * A_BYTES;
             const uint32_t sb = sbase + SmemLayout::b + stage * B_BYTES;
             tma_load_2d(sa, &tmA, kb * KE, w.row0, bar_full(stage));
-            tma_load_2d(sb, mb, kb * KE, rA, bar_full(stage));
-            tma_load_2d(sb + B_HALF, mb, kb * KE, rB, bar_full(stage));
+            tma_load_2d(sb, mb, wx(kb), wy(rA, kb), bar_full(stage));
+            tma_load_2d(sb + B_HALF, mb, wx(kb), wy(rB, kb), bar_full(stage));
           }
           if (++stage == (M2 ? STAGES_M2 : STAGES)) {
             stage = 0;
@@ -1070,6 +1076,9 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
                               int32_t* dev_status, const float* row_scale, void* stream,
                               const FuseIn* fuse = nullptr, unsigned long long timeout_ns = TIMEOUT_NS,
                               bool pairs = false) {
+  // MOE_W_TILED in dtype: the weights are in the tile layout of moe_pack_weights
+  const bool tiled = (static_cast<int>(dtype) & MOE_W_TILED) != 0;
+  dtype = static_cast<moe_dtype_t>(static_cast<int>(dtype) & ~MOE_W_TILED);
   const bool fp8 = dtype == MOE_E4M3;
   const bool swiglu = epilogue == MOE_EPI_SWIGLU;
   if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
@@ -1096,6 +1105,10 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
        reinterpret_cast<uintptr_t>(out)) & 15)
     return MOE_ERR_ARG;
   if ((uint64_t)num_w * n_dim > 0x7fffffffull) return MOE_ERR_ARG;
+  // tile layout: box row coordinates up to num_w * n_dim * k_dim / KE stay in int
+  const uint64_t ke_el = fp8 ? 128 : 64;
+  if (tiled && (pairs || (uint64_t)std::max(num_w, 1) * n_dim * (k_dim / ke_el) > 0x7fffffffull))
+    return pairs ? MOE_ERR_UNSUPPORTED : MOE_ERR_ARG;
   Args args;
   args.cu = cu_seqlens;
   args.max_tokens = max_tokens;
@@ -1121,6 +1134,7 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   args.T = fuse ? fuse->T : 0;
   args.K = fuse ? fuse->K : 1;
   args.timeout_ns = timeout_ns;
+  args.w_tiled = tiled ? 1 : 0;
   cudaStream_t s = as_stream(stream);
   // BF16 on CTA pairs with the 2-SM MMA (gemm2sm.cu), when asked for
   if (pairs) {
@@ -1134,9 +1148,12 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
   if (!make_map(&mat, a, fp8, k_dim, rows_cap, NS)) return MOE_ERR_CUDA;
   const void* wb = num_w > 0 ? w : w_extra;
   const uint64_t wrows = num_w > 0 ? (uint64_t)num_w * n_dim : (uint64_t)n_dim;
-  if (!make_map(&mb, wb, fp8, k_dim, wrows)) return MOE_ERR_CUDA;
+  // weights: [rows, k_dim] row-major, or the tile layout viewed as [rows * k_dim / KE, KE]
+  const uint64_t kt = tiled ? (uint64_t)k_dim / ke_el : 1;
+  const uint64_t w_inner = tiled ? ke_el : (uint64_t)k_dim;
+  if (!make_map(&mb, wb, fp8, w_inner, wrows * kt)) return MOE_ERR_CUDA;
   if (w_extra) {
-    if (!make_map(&mbx, w_extra, fp8, k_dim, n_dim)) return MOE_ERR_CUDA;
+    if (!make_map(&mbx, w_extra, fp8, w_inner, (uint64_t)n_dim * kt)) return MOE_ERR_CUDA;
   } else {
     mbx = mb;
   }
@@ -1167,6 +1184,44 @@ static moe_status_t gemm_impl(const void* a, const float* a_scales, const int32_
 }
 }  // namespace gg
 }  // namespace moe
+
+// Tile layout (moe_pack_weights): a copy of w [rows, k] (rows % 128 == 0, rows of 128-byte
+// tile rows) in which the tile of 128 rows x 128 bytes at (row block rb, K block kb) is
+// contiguous, at byte ((rb * kbn + kb) * 128) * 128, kbn = row bytes / 128.  Each thread
+// writes 16-byte pieces in destination order (a tile row is 8 of them).
+namespace moe {
+__global__ void __launch_bounds__(256) pack_tiles_kernel(const uint4* __restrict__ w, uint4* __restrict__ t,
+                                                         uint64_t total, uint32_t k16) {
+  const uint32_t kbn = k16 / 8;
+  for (uint64_t d = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; d < total;
+       d += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t j = static_cast<uint32_t>(d & 7);
+    const uint32_t rr = static_cast<uint32_t>((d >> 3) & 127);
+    const uint64_t tile = d >> 10;
+    const uint64_t kb = tile % kbn, rb = tile / kbn;
+    t[d] = w[(rb * 128 + rr) * k16 + kb * 8 + j];
+  }
+}
+}  // namespace moe
+
+extern "C" moe_status_t moe_pack_weights(const void* w, int E, int N, int K, moe_dtype_t dtype, void* w_tiled,
+                                         void* stream) {
+  if (dtype != MOE_BF16 && dtype != MOE_E4M3) return MOE_ERR_ARG;
+  if (E < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 128 != 0) return MOE_ERR_ARG;
+  const uint64_t esz = dtype == MOE_E4M3 ? 1 : 2;
+  const uint64_t bytes = (uint64_t)E * N * K * esz;
+  if (bytes == 0) return MOE_OK;
+  if (!w || !w_tiled || ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(w_tiled)) & 15))
+    return MOE_ERR_ARG;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(w), b0 = reinterpret_cast<uintptr_t>(w_tiled);
+  if (a0 < b0 + bytes && b0 < a0 + bytes) return MOE_ERR_ARG;   // not in place, no overlap
+  const uint64_t total = bytes / 16;
+  const int blocks = (int)std::min<uint64_t>((total + 255) / 256, (uint64_t)moe::num_sms() * 8);
+  moe::pack_tiles_kernel<<<blocks, 256, 0, moe::as_stream(stream)>>>(
+      static_cast<const uint4*>(w), static_cast<uint4*>(w_tiled), total, static_cast<uint32_t>(K * esz / 16));
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
 
 extern "C" moe_status_t moe_grouped_gemm_ex(const void* a, const float* a_scales, const int32_t* cu_seqlens,
                                             int num_segments, int rows_cap, int k_dim, int n_dim, const void* w,

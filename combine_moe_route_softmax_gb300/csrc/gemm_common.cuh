@@ -65,6 +65,7 @@ struct Args {
   int32_t* counters;        // [T, n_dim / 128], zero on entry, left zero
   int T, K;
   int stream;               // 1: segments of at most NS rows go to streaming CTAs
+  int w_tiled;              // 1: weights in the tile layout of moe_pack_weights (single-CTA kernel)
   int common_off;           // shared-memory offset of the common tail
   unsigned long long timeout_ns;  // limit of each pipeline wait (TIMEOUT_NS; shorter only in tests)
 };

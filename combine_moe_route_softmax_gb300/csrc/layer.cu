@@ -32,7 +32,7 @@ inline bool plan_layer(const moe_layer_desc_t* d, LayerPlan* p) {
       (d->fuse_combine != 0 && d->fuse_combine != 1) ||
       (d->combine_fq_format != 0 && d->combine_fq_format != 1) ||
       (d->dispatch_fq_format != 0 && d->dispatch_fq_format != 1) ||
-      (d->gemm_pairs != 0 && d->gemm_pairs != 1) ||
+      (d->gemm_pairs != 0 && d->gemm_pairs != 1) || (d->weight_tiles != 0 && d->weight_tiles != 1) ||
       (d->dtype != MOE_BF16 && d->dtype != MOE_E4M3))
     return false;
   const size_t T = d->T, K = d->K, H = d->H, I = d->I;
@@ -110,7 +110,7 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   if (fp8 && dispatch_scale) return MOE_ERR_UNSUPPORTED;   // the FP8 path already quantises the dispatch
   const bool fq4 = fq_scale && d->combine_fq_format == 1;
   if (fq4 && d->fuse_combine) return MOE_ERR_UNSUPPORTED;
-  if (d->gemm_pairs && (fp8 || d->max_tokens > 0 || d->fuse_combine)) return MOE_ERR_UNSUPPORTED;
+  if (d->gemm_pairs && (fp8 || d->max_tokens > 0 || d->fuse_combine || d->weight_tiles)) return MOE_ERR_UNSUPPORTED;
   if (d->has_shared && (!w->shared_w13 || !w->shared_w2 ||
                         (fp8 && (!w->shared_w13_scales || !w->shared_w2_scales))))
     return MOE_ERR_ARG;
@@ -126,6 +126,8 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
   const void* sx2 = d->has_shared ? w->shared_w2 : nullptr;
   const float* sx13s = d->has_shared ? w->shared_w13_scales : nullptr;
   const float* sx2s = d->has_shared ? w->shared_w2_scales : nullptr;
+  // the grouped GEMMs' dtype argument, with the weight layout
+  const moe_dtype_t gdt = static_cast<moe_dtype_t>(d->dtype | (d->weight_tiles ? MOE_W_TILED : 0));
   if (d->max_tokens > 0) {
     // batched layout: same steps, segment s in rows [s*max_tokens, s*max_tokens + masked_m[s])
     const int mt = d->max_tokens;
@@ -137,16 +139,16 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                       d->dispatch_fq_format);
     if (st != MOE_OK) return st;
     st = moe_grouped_gemm_batched(v.xp, v.xp_scales, v.masked_m, p.nseg, mt, d->H, 2 * d->I, w->w13,
-                                  w->w13_scales, d->E, sx13, sx13s, d->dtype, MOE_EPI_SWIGLU, v.hs, v.hs_scales,
+                                  w->w13_scales, d->E, sx13, sx13s, gdt, MOE_EPI_SWIGLU, v.hs, v.hs_scales,
                                   dev_status, nullptr, stream);
     if (st != MOE_OK) return st;
     if (d->fuse_combine)
       return moe_grouped_gemm_combine(v.hs, v.hs_scales, v.masked_m, p.nseg, mt, 0, d->I, d->H, w->w2,
-                                      w->w2_scales, d->E, sx2, sx2s, d->dtype, v.y, wd ? v.row_weights : nullptr,
+                                      w->w2_scales, d->E, sx2, sx2s, gdt, v.y, wd ? v.row_weights : nullptr,
                                       v.src_row, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, v.shared_map,
                                       fq_scale, out, v.counters, dev_status, stream);
     st = moe_grouped_gemm_batched(v.hs, v.hs_scales, v.masked_m, p.nseg, mt, d->I, d->H, w->w2, w->w2_scales,
-                                  d->E, sx2, sx2s, d->dtype, MOE_EPI_NONE, v.y, nullptr, dev_status,
+                                  d->E, sx2, sx2s, gdt, MOE_EPI_NONE, v.y, nullptr, dev_status,
                                   wd ? v.row_weights : nullptr, stream);
     if (st != MOE_OK) return st;
     if (fq4)
@@ -174,16 +176,16 @@ extern "C" moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_l
                        v.shared_map, fq_scale, out, stream);
   }
   st = moe_grouped_gemm(v.xp, v.xp_scales, v.cu_seqlens, p.nseg, p.cap, d->H, 2 * d->I, w->w13, w->w13_scales, d->E,
-                        sx13, d->has_shared ? w->shared_w13_scales : nullptr, d->dtype, MOE_EPI_SWIGLU, v.hs,
+                        sx13, d->has_shared ? w->shared_w13_scales : nullptr, gdt, MOE_EPI_SWIGLU, v.hs,
                         v.hs_scales, dev_status, stream);
   if (st != MOE_OK) return st;
   if (d->fuse_combine)
     return moe_grouped_gemm_combine(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, 0, p.cap, d->I, d->H, w->w2,
-                                    w->w2_scales, d->E, sx2, sx2s, d->dtype, v.y, wd ? v.row_weights : nullptr,
+                                    w->w2_scales, d->E, sx2, sx2s, gdt, v.y, wd ? v.row_weights : nullptr,
                                     v.src_row, v.inv_map, wd ? nullptr : topk_w, d->T, d->K, v.shared_map, fq_scale,
                                     out, v.counters, dev_status, stream);
   st = moe_grouped_gemm_ex(v.hs, v.hs_scales, v.cu_seqlens, p.nseg, p.cap, d->I, d->H, w->w2, w->w2_scales, d->E,
-                           sx2, d->has_shared ? w->shared_w2_scales : nullptr, d->dtype, MOE_EPI_NONE, v.y, nullptr,
+                           sx2, d->has_shared ? w->shared_w2_scales : nullptr, gdt, MOE_EPI_NONE, v.y, nullptr,
                            dev_status, wd ? v.row_weights : nullptr, stream);
   if (st != MOE_OK) return st;
   // with the router weights applied in the down projection the combine only sums

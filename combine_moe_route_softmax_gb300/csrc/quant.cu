@@ -109,7 +109,7 @@ extern "C" moe_status_t moe_quantize_weight_fp8(const uint16_t* w, int mats, int
   return MOE_OK;
 }
 
-extern "C" int moe_abi_version(void) { return 5; }
+extern "C" int moe_abi_version(void) { return 6; }
 
 extern "C" const char* moe_status_string(moe_status_t s) {
   switch (s) {

@@ -47,6 +47,9 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_BF16 = 0, MOE_E4M3 = 1 } moe_dtype_t;
+/* ORed into the dtype argument of moe_grouped_gemm, _ex, _batched and _combine: w and
+ * w_extra are in the tile layout of moe_pack_weights (ABI 6). */
+#define MOE_W_TILED 0x100
 typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 
 /* Bits of the device status word. */
@@ -59,7 +62,8 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1 } moe_epilogue_t;
 /* Version of this ABI (bumped on any signature change; 2 added the weight_in_down and
  * dispatch fake-quant options, 3 the batched expert layout, 4 the NVFP4 combine
  * and dispatch fake-quant (moe_combine_nvfp4, the dispatch_format arguments,
- * moe_layer_desc_t.combine_fq_format / dispatch_fq_format), 5 moe_grouped_gemm_pairs). */
+ * moe_layer_desc_t.combine_fq_format / dispatch_fq_format), 5 moe_grouped_gemm_pairs,
+ * 6 the tiled weight layout: moe_pack_weights, MOE_W_TILED, moe_layer_desc_t.weight_tiles). */
 int moe_abi_version(void);
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t s);
@@ -237,6 +241,31 @@ moe_status_t moe_grouped_gemm_pairs(const void* a, const int32_t* cu_seqlens, in
                                     moe_epilogue_t epilogue, void* out, int32_t* dev_status,
                                     const float* row_scale, void* stream);
 
+/* Tiled weight layout (ABI 6; an addition of this library, the pages have no counterpart).
+ * The grouped GEMM reads a weight matrix as boxes of 128 rows x 128 bytes of K (64 BF16 or
+ * 128 E4M3 elements); in the row-major layout such a box is 128 pieces of 128 bytes, one
+ * per row, a row (k_dim elements) apart, and a segment of a few rows streams its weights
+ * as a sequence of such scattered pieces.  moe_pack_weights writes a copy of the weights
+ * in which every box is 16 contiguous KB:
+ *   w        [E, N, K] (K-major rows) of dtype, N % 128 == 0, K % 128 == 0.
+ *   w_tiled  out, the same number of bytes: box (e, nb, kb) -- rows [128 nb, 128 nb + 128)
+ *            of matrix e, bytes [128 kb, 128 kb + 128) of each row -- at byte offset
+ *            ((e * (N / 128) + nb) * (K * esize / 128) + kb) * 16384, its 128 rows of
+ *            128 bytes in order (esize = 2 for BF16, 1 for E4M3).
+ * The shared expert's matrix is packed the same way with E = 1.  The E4M3 weight scales
+ * keep their layout.  A one-time preparation of model weights; asynchronous on stream.
+ * Errors: MOE_ERR_ARG for bad sizes, a null or misaligned (16 bytes) pointer, or
+ * overlapping w and w_tiled. */
+moe_status_t moe_pack_weights(const void* w, int E, int N, int K, moe_dtype_t dtype, void* w_tiled, void* stream);
+
+/* A grouped GEMM call whose dtype argument carries MOE_W_TILED (moe_grouped_gemm, _ex,
+ * _batched, _combine) reads w and w_extra in this layout; every other argument and the
+ * results, bit for bit, are those of the row-major call.  On the Zipf-routed prefill batch
+ * the weight stream of the many experts with a few rows is faster from contiguous boxes.
+ * Errors: those of the call, and MOE_ERR_ARG when num_w * n_dim * k_dim / (64 BF16 or 128
+ * E4M3 elements) exceeds 2^31 - 1; moe_grouped_gemm_pairs has no dtype argument and reads
+ * row-major weights only. */
+
 /* ------------------------------------------------------------ batched expert layout
  * The expert-batched activation format ([DeepEP]: the low-latency dispatch hands the
  * experts one fixed block of rows per expert, 3-D [E, max_tokens, H], while the
@@ -405,6 +434,9 @@ typedef struct {
   int gemm_pairs;     /* 1: both grouped GEMMs on SM pairs (moe_grouped_gemm_pairs; BF16,
                          contiguous layout, not with fuse_combine, else MOE_ERR_UNSUPPORTED);
                          same output bit for bit; 0: moe_grouped_gemm / _ex (ABI 5) */
+  int weight_tiles;   /* 1: w13, w2, shared_w13 and shared_w2 are in the tile layout of
+                         moe_pack_weights (any layout and dtype; not with gemm_pairs, else
+                         MOE_ERR_UNSUPPORTED); same output bit for bit; 0: row-major (ABI 6) */
 } moe_layer_desc_t;
 
 typedef struct {

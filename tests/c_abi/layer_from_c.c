@@ -46,7 +46,7 @@ static uint16_t* random_bf16(size_t n, float scale) {
 
 int main(void) {
   const int T = 96, H = 256, I = 128, E = 16, K = 4;
-  CHECK(moe_abi_version() == 5);
+  CHECK(moe_abi_version() == 6);
 
   float* h_logits = (float*)malloc((size_t)T * E * 4);
   for (int i = 0; i < T * E; ++i) h_logits[i] = lcg_uniform() * 3.0f;

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_host_only_calls(lib):
-    assert lib.moe_abi_version() == 5
+    assert lib.moe_abi_version() == 6
     assert lib.moe_status_string(2) == b"workspace too small"
     # scratch sized from the inputs: grows with T, K and E
     a = lib.moe_permute_workspace_bytes(128, 8, 256, 1)
@@ -110,3 +110,36 @@ def test_argument_errors_launch_nothing(lib):
                                         None, None, None, None, 4, 2, None, None, None, None, None, None) == 1
     assert lib.moe_grouped_gemm_combine(None, None, None, 1, 0, 16, 128, 256, None, None, 1, None, None, 0, None,
                                         None, None, None, None, 4, 33, None, None, None, None, None, None) == 1
+
+
+def test_weight_tiles_host_checks(lib):
+    """The tile layout's host-side checks (nothing is launched): the layer descriptor flag is
+    0 or 1 and does not change the workspace; moe_pack_weights refuses bad sizes, misaligned
+    or overlapping buffers and does nothing for an empty tensor; a tiled grouped GEMM whose box
+    coordinates would pass 2^31 is refused; SM pairs with tiled weights are refused."""
+    d = moe.LayerDesc(128, 7168, 2048, 256, 8, moe.MOE_BF16, 1)
+    n0 = lib.moe_layer_workspace_bytes(ctypes.byref(d))
+    d.weight_tiles = 1
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(d)) == n0 > 0
+    d.weight_tiles = 2
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(d)) == 0
+    a, b = 1 << 30, 1 << 34          # device-looking addresses, never dereferenced
+    assert lib.moe_pack_weights(a, 0, 256, 256, moe.MOE_BF16, b, None) == 0
+    assert lib.moe_pack_weights(a, 2, 200, 256, moe.MOE_BF16, b, None) == 1       # N % 128
+    assert lib.moe_pack_weights(a, 2, 256, 192, moe.MOE_BF16, b, None) == 1       # K % 128
+    assert lib.moe_pack_weights(a, 2, 256, 256, 7, b, None) == 1                  # dtype
+    assert lib.moe_pack_weights(a + 8, 2, 256, 256, moe.MOE_BF16, b, None) == 1   # alignment
+    assert lib.moe_pack_weights(a, 2, 256, 256, moe.MOE_BF16, a + 4096, None) == 1  # overlap
+    assert lib.moe_pack_weights(None, 2, 256, 256, moe.MOE_BF16, b, None) == 1
+    # 70000 matrices of 4096 x 7168 BF16: 3.2e10 boxes rows, past int32
+    big = lib.moe_grouped_gemm(a, None, b, 1, 128, 7168, 4096, a, None, 70000, None, None,
+                               moe.MOE_BF16 | moe.MOE_W_TILED, moe.MOE_EPI_NONE, b, None, None, None)
+    assert big == 1
+    dp = moe.LayerDesc(128, 7168, 2048, 256, 8, moe.MOE_BF16, 0)
+    dp.gemm_pairs = 1
+    dp.weight_tiles = 1
+    n = lib.moe_layer_workspace_bytes(ctypes.byref(dp))
+    wts = moe.LayerWeights(a, None, a, None, None, None, None, None)
+    code = lib.moe_layer_forward(ctypes.byref(dp), ctypes.byref(wts), None, None, a, a, a, None, None, a, b, n,
+                                 None, None)
+    assert code == 3

@@ -27,7 +27,7 @@ WORKERS = min(16, os.cpu_count() or 1)   # experts the oracle computes at once (
 class Setup:
     """A workload's inputs and weights on the GPU plus a MoeLayer over them."""
 
-    def __init__(self, w, seed=0, weights=None):
+    def __init__(self, w, seed=0, weights=None, weight_tiles=False):
         self.w = w
         self.logits = synth.router_logits(w, seed, device="cuda")
         self.x = synth.hidden(w, seed, device="cuda")
@@ -43,7 +43,8 @@ class Setup:
                 kw.update(shared_w13=qs13, shared_w2=qs2, shared_w13_scales=ss13, shared_w2_scales=ss2)
         else:
             kw = dict(w13=self.w13, w2=self.w2, shared_w13=self.s13, shared_w2=self.s2)
-        self.layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_E4M3 if w.dtype == "e4m3" else moe.MOE_BF16, **kw)
+        self.layer = moe.MoeLayer(w.T, w.H, w.I, w.E, w.K, moe.MOE_E4M3 if w.dtype == "e4m3" else moe.MOE_BF16,
+                                  weight_tiles=weight_tiles, **kw)
         self.topk_idx = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
         self.topk_w = torch.empty(w.T, w.K, dtype=torch.float32, device="cuda")
         self.out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
@@ -120,10 +121,11 @@ def test_layer_every_token(name, T, H, I, E, K):
 
 
 def test_layer_prefill_full_size_every_token():
-    """Full prefill size: all 8192 tokens against the fp64 reference (the whole layer
-    output is also checked as the re-sum of the layer's own expert rows)."""
+    """Full prefill size, in the benchmark's configuration (weights in the tile layout): all
+    8192 tokens against the fp64 reference (the whole layer output is also checked as the
+    re-sum of the layer's own expert rows)."""
     need_gpu()
-    s = Setup(WORKLOADS["prefill"])
+    s = Setup(WORKLOADS["prefill"], weight_tiles=True)
     check_layer(s, np.arange(8192), TOL["bf16"], label="prefill (every token)")
     # the expert-major layout the layer built is the oracle's, bit for bit
     v = s.layer.views
@@ -167,9 +169,10 @@ def test_layer_decode_full_size_every_token():
     quantised by the oracle), and against the fp64 layer on the unquantised BF16 masters at
     the bound E4M3's rounding allows (below).  The 6e-2 figure is the MoonEP page's test
     tolerance ("BF16 integration of MoonEP balanced EP backend", Test Result: atol = rtol =
-    6e-2 against a per-token reference MoE), set there for BF16 operands."""
+    6e-2 against a per-token reference MoE), set there for BF16 operands.  Weights in the
+    tile layout, as the benchmark runs."""
     need_gpu()
-    s = Setup(WORKLOADS["decode"])
+    s = Setup(WORKLOADS["decode"], weight_tiles=True)
     check_layer(s, np.arange(128), TOL["e4m3"], label="decode vs the FP8-operand reference")
     # Against the BF16 masters the difference is E4M3's own rounding: x, W13, h and W2 are
     # each rounded with a relative error of rms 2^-4 / sqrt(3) = 3.6 % (three mantissa

@@ -248,6 +248,8 @@ def moe_pack_weights(w, out=None, stream=None):
     mats = w.numel() // (n * k)
     if out is None:
         out = torch.empty_like(w)
+    _dev(out)
+    assert out.numel() * out.element_size() == w.numel() * w.element_size(), "out must hold w's bytes"
     dt = MOE_E4M3 if w.dtype == torch.uint8 else MOE_BF16
     _check("moe_pack_weights", lib().moe_pack_weights(_ptr(w), mats, n, k, dt, _ptr(out), _stream(stream)))
     return out

@@ -125,6 +125,33 @@ int main(void) {
     for (int a = 0; a < K; ++a)
       for (int b2 = a + 1; b2 < K; ++b2) CHECK(h_idx[t * K + a] != h_idx[t * K + b2]);
 
+  /* the same layer on weights packed into the tile layout: the same output, bit for bit */
+  void *t13 = NULL, *t2 = NULL, *ts13 = NULL, *ts2 = NULL;
+  uint16_t* out_t = NULL;
+  CHECK(cudaMalloc(&t13, (size_t)E * 2 * I * H * 2) == cudaSuccess);
+  CHECK(cudaMalloc(&t2, (size_t)E * H * I * 2) == cudaSuccess);
+  CHECK(cudaMalloc(&ts13, (size_t)2 * I * H * 2) == cudaSuccess);
+  CHECK(cudaMalloc(&ts2, (size_t)H * I * 2) == cudaSuccess);
+  CHECK(cudaMalloc((void**)&out_t, (size_t)T * H * 2) == cudaSuccess);
+  CHECK(moe_pack_weights(w13, E, 2 * I, H, MOE_BF16, t13, NULL) == MOE_OK);
+  CHECK(moe_pack_weights(w2, E, H, I, MOE_BF16, t2, NULL) == MOE_OK);
+  CHECK(moe_pack_weights(s13, 1, 2 * I, H, MOE_BF16, ts13, NULL) == MOE_OK);
+  CHECK(moe_pack_weights(s2, 1, H, I, MOE_BF16, ts2, NULL) == MOE_OK);
+  CHECK(moe_pack_weights(w13, E, 2 * I, H, MOE_BF16, w13, NULL) == MOE_ERR_ARG);   /* not in place */
+  moe_layer_desc_t dt = d;
+  dt.weight_tiles = 1;
+  moe_layer_weights_t wt = w;
+  wt.w13 = t13; wt.w2 = t2; wt.shared_w13 = ts13; wt.shared_w2 = ts2;
+  CHECK(moe_layer_forward(&dt, &wt, logits, NULL, topk_idx, topk_w, x, NULL, NULL, out_t, ws, ws_bytes, status,
+                          NULL) == MOE_OK);
+  uint16_t* h_out = (uint16_t*)malloc((size_t)T * H * 2);
+  uint16_t* h_out_t = (uint16_t*)malloc((size_t)T * H * 2);
+  CHECK(cudaMemcpy(h_out, out, (size_t)T * H * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+  CHECK(cudaMemcpy(h_out_t, out_t, (size_t)T * H * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+  CHECK(memcmp(h_out, h_out_t, (size_t)T * H * 2) == 0);
+  CHECK(cudaMemcpy(&h_status, status, 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+  CHECK(h_status == 0);
+
   printf("ok\n");
   return 0;
 }

@@ -191,3 +191,23 @@ def test_layer_pairs_refuse_tiles():
                       torch.empty(w.T, w.K, dtype=torch.float32, device="cuda"),
                       logits=synth.router_logits(w, 0, device="cuda"))
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_gemm_tiled_extra_segment_only(swiglu):
+    """num_w = 0: the only weights are w_extra (a layer's shared expert alone), tiled."""
+    need_gpu()
+    k, n = 384, 512
+    g = torch.Generator().manual_seed(23)
+    a = torch.randn(300, k, generator=g).to(torch.bfloat16).cuda()
+    wx = (torch.randn(n, k, generator=g) / k ** 0.5).to(torch.bfloat16).cuda()
+    w0 = torch.empty(0, n, k, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 300], dtype=torch.int32, device="cuda")
+    epi = moe.MOE_EPI_SWIGLU if swiglu else moe.MOE_EPI_NONE
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_r, _ = moe.moe_grouped_gemm(a, cu, w0, w_extra=wx, epilogue=epi, dev_status=st)
+    o_t, _ = moe.moe_grouped_gemm(a, cu, w0, w_extra=moe.moe_pack_weights(wx), epilogue=epi, dev_status=st,
+                                  tiled=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert same_bits(o_r, o_t)

@@ -518,6 +518,13 @@ def run_ours(args, rank, world, local_rank):
     kernels = {}
     for name in STAGES:
         k = {"ms": round(stage_ms[name], 4)}
+        if args.fuse_combine and name == "combine":
+            # the combine runs inside the down projection's launch: no stage of its own
+            k["fused_into"] = "gemm_down"
+            kernels[name] = k
+            continue
+        if args.fuse_combine and name == "gemm_down":
+            k["includes"] = "the combine"
         wk = work[name]
         if "flops" in wk:
             k["tflops"] = round(wk["flops"] / (stage_ms[name] * 1e-3) / 1e12, 1)
